@@ -1,0 +1,352 @@
+"""Seeded synthetic inputs for the masked-attention and split-KV decode workloads.
+
+This module is shared by the CPU oracle's tests, the GPU parity tests and the
+bench. It holds no attention arithmetic: only a counter-based random number
+generator, Box-Muller normals, round-to-nearest-even conversion to bf16, mask
+*descriptions* (pattern parameters or explicit bit arrays) and the workload
+shapes. Both the oracle and the CUDA path evaluate these descriptions with code
+of their own.
+
+Random numbers
+--------------
+SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+generators", OOPSLA 2014): state_n = key + n * 0x9E3779B97F4A7C15, output
+mix(state_n) with the published finaliser. Each (seed, stream) pair gets its
+own key, and draw number i of a stream is output n = i + 1, so any draw can be
+computed independently of the others.
+
+Streams used (seed 0 for every workload):
+  1 Q, 2 K, 3 V, 4 mask block choice, 5 decode lengths, 6 mask elements.
+
+Normals: Box-Muller on the pair of draws (2i, 2i+1): u1 = ((x >> 11) + 1) / 2^53
+in (0, 1], u2 = (y >> 11) / 2^53, z = sqrt(-2 ln u1) cos(2 pi u2), evaluated in
+float64 and rounded to float32; bf16 inputs round that float32 value to
+bfloat16 with round-to-nearest-even.
+
+Mask conventions
+----------------
+A mask head is a [Lq, Lk] 0/1 matrix, 1 = the key may be attended. It is given
+either as a pattern
+
+    valid(i, j) = (not causal or j <= i)
+                  and (win_lo <= j - i <= win_hi  or  j < n_global_cols)
+
+or as dense bits: uint64 words [Lq, ceil(Lk / 64)], element (i, j) in word
+j >> 6, bit j & 63 (bits at j >= Lk are zero), or as dense uint8 [Lq, Lk].
+Head h of the attention uses mask head head_map[h].
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+
+_M64 = (1 << 64) - 1
+_GAMMA = 0x9E3779B97F4A7C15
+_C1 = 0xBF58476D1CE4E5B9
+_C2 = 0x94D049BB133111EB
+
+STREAM_Q, STREAM_K, STREAM_V = 1, 2, 3
+STREAM_MASK_BLOCKS, STREAM_LENGTHS, STREAM_MASK_ELEMS = 4, 5, 6
+
+BIG = 1 << 40  # "unbounded" window edge for patterns
+
+
+def _mix_int(z: int) -> int:
+    z &= _M64
+    z = ((z ^ (z >> 30)) * _C1) & _M64
+    z = ((z ^ (z >> 27)) * _C2) & _M64
+    return z ^ (z >> 31)
+
+
+def stream_key(seed: int, stream: int) -> int:
+    """SplitMix64 starting state for one (seed, stream) pair."""
+    return _mix_int(seed * _GAMMA + stream * 0xD1B54A32D192ED03 + 1)
+
+
+def splitmix64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
+    """Draws start .. start+count-1 of a stream, as uint64."""
+    key = np.uint64(stream_key(seed, stream))
+    n = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    z = key + n * np.uint64(_GAMMA)
+    z = (z ^ (z >> np.uint64(30))) * np.uint64(_C1)
+    z = (z ^ (z >> np.uint64(27))) * np.uint64(_C2)
+    return z ^ (z >> np.uint64(31))
+
+
+def uniform01(x: np.ndarray) -> np.ndarray:
+    """53-bit uniform in [0, 1)."""
+    return (x >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+
+
+def normals_f32(seed: int, stream: int, count: int, chunk: int = 1 << 23) -> np.ndarray:
+    out = np.empty(count, dtype=np.float32)
+    for s in range(0, count, chunk):
+        n = min(chunk, count - s)
+        x = splitmix64(seed, stream, 2 * s, 2 * n)
+        u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+        u2 = uniform01(x[1::2])
+        out[s:s + n] = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)).astype(np.float32)
+    return out
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = ((b >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((b + r) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float32."""
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class Tensor:
+    """One input tensor: float32 values (exact) and, for bf16 inputs, the bit patterns."""
+    f32: np.ndarray
+    bf16: Optional[np.ndarray]  # uint16, same shape, or None for fp32 inputs
+
+    @property
+    def shape(self):
+        return self.f32.shape
+
+
+def make_tensor(seed: int, stream: int, shape, dtype: str, mult: float = 1.0) -> Tensor:
+    v = normals_f32(seed, stream, int(np.prod(shape))).reshape(shape)
+    if mult != 1.0:
+        v = (v * np.float32(mult)).astype(np.float32)
+    if dtype == "bf16":
+        bits = f32_to_bf16_bits(v)
+        return Tensor(bf16_bits_to_f32(bits), bits)
+    if dtype == "f32":
+        return Tensor(v, None)
+    raise ValueError(dtype)
+
+
+@dataclass
+class MaskHead:
+    """One [Lq, Lk] mask head, as a pattern or as explicit data."""
+    kind: str  # "pattern" | "bits" | "u8"
+    causal: int = 0
+    win_lo: int = -BIG
+    win_hi: int = BIG
+    n_global_cols: int = 0
+    data: Optional[np.ndarray] = None  # bits: uint64 [Lq, W]; u8: uint8 [Lq, Lk]
+
+
+def pattern(causal=False, win_lo=-BIG, win_hi=BIG, n_global_cols=0) -> MaskHead:
+    return MaskHead("pattern", int(bool(causal)), int(win_lo), int(win_hi), int(n_global_cols))
+
+
+def pack_bits(dense_u8: np.ndarray) -> np.ndarray:
+    """[..., Lk] 0/1 -> uint64 words [..., ceil(Lk/64)], element j at word j>>6 bit j&63."""
+    Lk = dense_u8.shape[-1]
+    W = (Lk + 63) // 64
+    pad = np.zeros(dense_u8.shape[:-1] + (W * 64,), dtype=np.uint8)
+    pad[..., :Lk] = dense_u8 != 0
+    packed = np.packbits(pad, axis=-1, bitorder="little")  # bytes, little bit order
+    return np.ascontiguousarray(packed).view("<u8").astype(np.uint64).reshape(dense_u8.shape[:-1] + (W,))
+
+
+def unpack_bits(bits: np.ndarray, Lk: int) -> np.ndarray:
+    b = np.ascontiguousarray(bits.astype("<u8")).view(np.uint8)
+    u = np.unpackbits(b, axis=-1, bitorder="little")
+    return u[..., :Lk].astype(np.uint8)
+
+
+def random_mask_u8(seed: int, stream: int, Lq: int, Lk: int, density: float, salt: int = 0) -> np.ndarray:
+    """Elementwise Bernoulli(density) mask; element (i, j) uses draw salt*Lq*Lk + i*Lk + j."""
+    x = splitmix64(seed, stream, salt * Lq * Lk, Lq * Lk)
+    thr = np.uint64(int(density * 9007199254740992.0))
+    return ((x >> np.uint64(11)) < thr).astype(np.uint8).reshape(Lq, Lk)
+
+
+def random_mask_bits(seed: int, stream: int, Lq: int, Lk: int, density: float,
+                     row_chunk: int = 512) -> np.ndarray:
+    """As random_mask_u8 with salt 0, packed to bits row-chunk by row-chunk."""
+    W = (Lk + 63) // 64
+    out = np.empty((Lq, W), dtype=np.uint64)
+    thr = np.uint64(int(density * 9007199254740992.0))
+    for r0 in range(0, Lq, row_chunk):
+        r1 = min(Lq, r0 + row_chunk)
+        x = splitmix64(seed, stream, r0 * Lk, (r1 - r0) * Lk)
+        u = ((x >> np.uint64(11)) < thr).astype(np.uint8).reshape(r1 - r0, Lk)
+        out[r0:r1] = pack_bits(u)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Workloads
+# ----------------------------------------------------------------------------
+
+@dataclass
+class MhaWorkload:
+    name: str
+    B: int
+    H: int
+    Lq: int
+    Lk: int
+    d: int
+    dtype: str  # "bf16" | "f32"
+    q: Tensor
+    k: Tensor
+    v: Tensor
+    mask_heads: List[MaskHead]
+    head_map: List[int]
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+
+def _qkv(seed, B, H, Lq, Lk, d, dtype, mult=1.0):
+    q = make_tensor(seed, STREAM_Q, (B, H, Lq, d), dtype, mult)
+    k = make_tensor(seed, STREAM_K, (B, H, Lk, d), dtype, mult)
+    v = make_tensor(seed, STREAM_V, (B, H, Lk, d), dtype, mult)
+    return q, k, v
+
+
+def tiny_causal(seed: int = 0) -> MhaWorkload:
+    """B=1, H=2, L=128, d=64, fp32, causal mask."""
+    B, H, L, d = 1, 2, 128, 64
+    q, k, v = _qkv(seed, B, H, L, L, d, "f32")
+    return MhaWorkload("tiny-causal-fp32 B1 H2 L128 d64", B, H, L, L, d, "f32", q, k, v,
+                       [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d))
+
+
+def bert_band(seed: int = 0, B: int = 8, H: int = 12, L: int = 512, d: int = 64, w: int = 64) -> MhaWorkload:
+    """BERT-base-shaped sliding window |i - j| <= w, bf16."""
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16")
+    return MhaWorkload(f"bert-band{w} bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       [pattern(win_lo=-w, win_hi=w)], [0] * H, 1.0 / math.sqrt(d))
+
+
+def bigbird_blocks(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3):
+    """Per mask head and query block: the sorted key-block lists of the BigBird recipe.
+
+    Window = {qb-1, qb, qb+1} within range, global = key blocks {0, 1}, and
+    n_rand blocks drawn without replacement from the remaining blocks (partial
+    Fisher-Yates on the ascending candidate list, draw index
+    ((h * nb + qb) * 8 + t) of the mask-block stream). Returns (full, rand):
+    lists [h][qb] of block indices.
+    """
+    nb = (L + blk - 1) // blk
+    full, rand = [], []
+    for h in range(Hm):
+        fh, rh = [], []
+        for qb in range(nb):
+            base = {b for b in (qb - 1, qb, qb + 1) if 0 <= b < nb} | {b for b in (0, 1) if b < nb}
+            cand = [b for b in range(nb) if b not in base]
+            x = splitmix64(seed, STREAM_MASK_BLOCKS, (h * nb + qb) * 8, 8)
+            chosen = []
+            for t in range(min(n_rand, len(cand))):
+                j = t + int(x[t] % np.uint64(len(cand) - t))
+                cand[t], cand[j] = cand[j], cand[t]
+                chosen.append(cand[t])
+            fh.append(sorted(base))
+            rh.append(sorted(chosen))
+        full.append(fh)
+        rand.append(rh)
+    return full, rand
+
+
+def bigbird_mask_bits(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3, p: float = 0.5):
+    """Dense bits [Hm, L, ceil(L/64)] of the BigBird-style mask.
+
+    Window and global blocks are all ones; inside each random block element
+    (h, i, j) is kept when draw (h * L + i) * L + j of the mask-element stream
+    is below p (53-bit uniform).
+    """
+    assert blk == 64, "bit packing below assumes 64-wide key blocks"
+    full, rand = bigbird_blocks(seed, Hm, L, blk, n_rand)
+    W = (L + 63) // 64
+    bits = np.zeros((Hm, L, W), dtype=np.uint64)
+    thr = np.uint64(int(p * 9007199254740992.0))
+    ones = np.uint64(0xFFFFFFFFFFFFFFFF)
+    for h in range(Hm):
+        for qb in range(len(full[h])):
+            r0, r1 = qb * blk, min(L, (qb + 1) * blk)
+            for kb in full[h][qb]:
+                bits[h, r0:r1, kb] = ones
+            for kb in rand[h][qb]:
+                rows = np.arange(r0, r1, dtype=np.uint64)
+                cols = np.arange(kb * blk, min(L, (kb + 1) * blk), dtype=np.uint64)
+                idx = ((np.uint64(h) * np.uint64(L) + rows[:, None]) * np.uint64(L) + cols[None, :])
+                key = np.uint64(stream_key(seed, STREAM_MASK_ELEMS))
+                z = key + (idx + np.uint64(1)) * np.uint64(_GAMMA)
+                z = (z ^ (z >> np.uint64(30))) * np.uint64(_C1)
+                z = (z ^ (z >> np.uint64(27))) * np.uint64(_C2)
+                z = z ^ (z >> np.uint64(31))
+                keep = ((z >> np.uint64(11)) < thr).astype(np.uint8)
+                packed = pack_bits(keep)[:, 0]
+                bits[h, r0:r1, kb] = packed
+    # clear bits past Lk in the last word
+    if L % 64:
+        bits[:, :, W - 1] &= np.uint64((1 << (L % 64)) - 1)
+    return bits
+
+
+def bigbird(seed: int = 0, B: int = 4, H: int = 16, L: int = 4096, d: int = 64) -> MhaWorkload:
+    """BigBird-style block-sparse mask, one mask head per attention head, bf16."""
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16")
+    bits = bigbird_mask_bits(seed, H, L)
+    heads = [MaskHead("bits", data=bits[h]) for h in range(H)]
+    return MhaWorkload(f"bigbird bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       heads, list(range(H)), 1.0 / math.sqrt(d))
+
+
+def longformer(seed: int = 0, B: int = 1, H: int = 32, L: int = 16384, d: int = 128,
+               window: int = 256, n_global: int = 16, density: float = 0.05) -> MhaWorkload:
+    """Longformer-style causal window + global columns; the last head uses a random mask.
+
+    Structured heads: causal and (i - j < window or j < n_global). The last
+    head replaces that mask with i.i.d. Bernoulli(density) over all L x L
+    elements (not combined with causal), draw i * L + j of the mask-element
+    stream.
+    """
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16", mult=0.5)
+    structured = pattern(causal=True, win_lo=-(window - 1), win_hi=BIG, n_global_cols=n_global)
+    rnd = MaskHead("bits", data=random_mask_bits(seed, STREAM_MASK_ELEMS, L, L, density))
+    head_map = [0] * (H - 1) + [1]
+    return MhaWorkload(f"longformer+random bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       [structured, rnd], head_map, 1.0 / math.sqrt(d))
+
+
+@dataclass
+class DecodeWorkload:
+    name: str
+    n_req: int
+    Hq: int
+    Hkv: int
+    d: int
+    dtype: str
+    q: Tensor  # [n_req, Hq, d]
+    k: Tensor  # [T, Hkv, d]
+    v: Tensor
+    kv_indptr: np.ndarray  # int32 [n_req + 1]
+    scale: float
+
+
+def decode_lengths(seed: int, n_req: int, lo: int = 512, hi: int = 32768) -> np.ndarray:
+    """Log-uniform lengths: floor(exp(ln lo + u * ln(hi/lo))) clamped to [lo, hi]."""
+    u = uniform01(splitmix64(seed, STREAM_LENGTHS, 0, n_req))
+    ln = np.floor(np.exp(math.log(lo) + u * math.log(hi / lo))).astype(np.int64)
+    return np.clip(ln, lo, hi)
+
+
+def gqa_decode(seed: int = 0, n_req: int = 64, Hq: int = 32, Hkv: int = 8, d: int = 128,
+               lo: int = 512, hi: int = 32768, lengths=None) -> DecodeWorkload:
+    """Ragged GQA decode: one query token per request, packed K/V [T, Hkv, d], bf16."""
+    lens = decode_lengths(seed, n_req, lo, hi) if lengths is None else np.asarray(lengths, np.int64)
+    indptr = np.zeros(n_req + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(lens)
+    T = int(indptr[-1])
+    assert T < 2**31
+    q = make_tensor(seed, STREAM_Q, (n_req, Hq, d), "bf16")
+    k = make_tensor(seed, STREAM_K, (T, Hkv, d), "bf16")
+    v = make_tensor(seed, STREAM_V, (T, Hkv, d), "bf16")
+    return DecodeWorkload(f"gqa-decode bf16 n_req{n_req} Hq{Hq} Hkv{Hkv} d{d} T{T}", n_req, Hq, Hkv, d,
+                          "bf16", q, k, v, indptr.astype(np.int32), 1.0 / math.sqrt(d))
