@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Benchmark of the masked-MHA / split-KV decode path on GB300.
+
+One JSON line on rank 0. Headline: valid-pair TFLOP/s of the masked MHA forward
+(4*d FLOPs per unmasked (q, k) pair per head) on the BERT-base-shaped band-64
+workload (B=8, H=12, L=512, d=64, bf16). The same line carries the split-KV GQA
+decode (KV-read GB/s) and the BigBird and Longformer workloads as secondary
+objects, each with its roofline fraction against the measured GB300 peaks.
+
+A step is one sta_mha_fwd call (mask encoded once, outside the timed region).
+L2 is flushed (a 256 MiB write, outside the CUDA events) before every timed
+launch. The device time is the sum of per-launch CUDA-event durations on the
+launching stream; `e2e` repeats the step through the public API with the
+inputs copied from pinned host memory and the outputs copied back inside the
+timed region.
+
+--impl reference times the CPU oracle (fp64, all host cores) on the same
+workload: the reference arm of this comparison is the plain restatement of
+the method, not a GPU system.
+
+Multi-GPU: the path shards into independent units but this build runs
+replicas only (every rank runs the same workload on its own GPU); value is
+the sum over ranks divided by the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha(name: str) -> str:
+    p = os.path.join(ROOT, "split_kv_decode_bsr_gb300", "csrc", name)
+    return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+
+
+def recorded_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_source_sha(kernel_file)
+    for line in open(p):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel_file and parts[1] == workload:
+            return float(parts[3]) if parts[2] == sha else None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(self.out)):
+            row = [c.strip() for c in row]
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                mx.append(float(row[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, row[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workloads
+
+
+def host_tensor(t):
+    """torch CPU tensor of a seeded input (bf16 bit patterns reinterpreted, or float32)."""
+    import torch
+
+    if t.bf16 is not None:
+        return torch.from_numpy(t.bf16.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(t.f32)
+
+
+def gpu_sources_for(mask_heads, dev):
+    """Mask descriptions of the seeded workloads as library mask sources (data uploaded)."""
+    import torch
+
+    import split_kv_decode_bsr_gb300 as sta
+
+    out = []
+    for m in mask_heads:
+        if m.kind == "pattern":
+            out.append(sta.MaskSource.pattern(m.causal, m.win_lo, m.win_hi, m.n_global_cols))
+        elif m.kind == "bits":
+            out.append(sta.MaskSource.dense_bits(torch.from_numpy(m.data.view(np.int64)).to(dev)))
+        else:
+            out.append(sta.MaskSource.dense_u8(torch.from_numpy(np.ascontiguousarray(m.data)).to(dev)))
+    return out
+
+
+def mha_workload(name):
+    import workloads as W
+
+    return {"bert-band": W.bert_band, "bigbird": W.bigbird, "longformer": W.longformer,
+            "tiny-causal": W.tiny_causal}[name]()
+
+
+def algorithmic_bytes_mha(wl, mask):
+    elt = 2 if wl.dtype == "bf16" else 4
+    qo = 2 * wl.B * wl.H * wl.Lq * wl.d * elt
+    kv = 2 * wl.B * wl.H * wl.Lk * wl.d * elt
+    lse = wl.B * wl.H * wl.Lq * 4
+    bitmaps = mask.n_part * 512 + (mask.n_full + mask.n_part) * 4 + 2 * (mask.Hm * mask.ot_rows + 1) * 4
+    return qo + kv + lse + bitmaps
+
+
+def valid_pairs(wl, mask_counts):
+    # mask_counts[h] = valid elements of mask head h
+    return sum(wl.B * mask_counts[wl.head_map[h]] for h in range(wl.H))
+
+
+class MhaBench:
+    def __init__(self, name, dev):
+        import torch
+
+        import split_kv_decode_bsr_gb300 as sta
+
+        self.sta = sta
+        self.wl = wl = mha_workload(name)
+        self.name = name
+        self.dev = dev
+        self.q, self.k, self.v = (host_tensor(t).to(dev) for t in (wl.q, wl.k, wl.v))
+        self.mask = sta.sta_encode_mask(gpu_sources_for(wl.mask_heads, dev), wl.Lq, wl.Lk)
+        # per-mask-head valid counts (encode each head alone: host-side bookkeeping only)
+        self.head_valid = [sta.sta_encode_mask(gpu_sources_for([m], dev), wl.Lq, wl.Lk).n_valid
+                           for m in wl.mask_heads]
+        self.pairs = valid_pairs(wl, self.head_valid)
+        self.flops = 4.0 * wl.d * self.pairs
+        self.bytes = algorithmic_bytes_mha(wl, self.mask)
+        self.kernel = sta.sta_mha_select_kernel(self.mask, wl.B, wl.H, wl.d,
+                                                torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((wl.B, wl.H, wl.Lq), dtype=torch.float32, device=dev)
+        self.hq, self.hk, self.hv = (x.cpu().pin_memory() for x in (self.q, self.k, self.v))
+        self.ho = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.hlse = torch.empty_like(self.lse, device="cpu").pin_memory()
+
+    def step(self, kernel=None):
+        self.sta.sta_mha_fwd(self.q, self.k, self.v, self.mask, head_map=self.wl.head_map, scale=self.wl.scale,
+                             kernel=kernel or "auto", o=self.o, lse=self.lse)
+
+    def step_e2e(self):
+        self.q.copy_(self.hq, non_blocking=True)
+        self.k.copy_(self.hk, non_blocking=True)
+        self.v.copy_(self.hv, non_blocking=True)
+        self.step()
+        self.ho.copy_(self.o, non_blocking=True)
+        self.hlse.copy_(self.lse, non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return sum(x.numel() * x.element_size() for x in (self.hq, self.hk, self.hv))
+
+    @property
+    def d2h_bytes(self):
+        return sum(x.numel() * x.element_size() for x in (self.ho, self.hlse))
+
+    def launches_per_step(self):
+        return 1
+
+
+class DecodeBench:
+    def __init__(self, dev):
+        import torch
+
+        import split_kv_decode_bsr_gb300 as sta
+        import workloads as W
+
+        self.sta = sta
+        self.wl = wl = W.gqa_decode()
+        self.dev = dev
+        self.q, self.k, self.v = (host_tensor(t).to(dev) for t in (wl.q, wl.k, wl.v))
+        self.ind_host = wl.kv_indptr
+        self.ind = torch.from_numpy(wl.kv_indptr).to(dev)
+        self.T = int(wl.kv_indptr[-1])
+        self.kv_bytes = self.T * wl.Hkv * wl.d * 2 * 2
+        self.bytes = self.kv_bytes + 2 * wl.n_req * wl.Hq * wl.d * 2 + wl.n_req * wl.Hq * 4
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((wl.n_req, wl.Hq), dtype=torch.float32, device=dev)
+        nbytes = sta.decode_workspace_bytes(self.ind_host, wl.n_req, wl.Hq, wl.Hkv, wl.d, 0)
+        self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.hq = self.q.cpu().pin_memory()
+        self.ho = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.hlse = torch.empty_like(self.lse, device="cpu").pin_memory()
+
+    def step(self):
+        self.sta.sta_decode_splitkv(self.q, self.k, self.v, self.ind, self.ind_host, scale=self.wl.scale,
+                                    num_splits=0, o=self.o, lse=self.lse, workspace=self.ws)
+
+    def step_e2e(self):
+        # serving shape: the KV cache stays resident; the new query tokens come in, outputs go out
+        self.q.copy_(self.hq, non_blocking=True)
+        self.step()
+        self.ho.copy_(self.o, non_blocking=True)
+        self.hlse.copy_(self.lse, non_blocking=True)
+
+    def launches_per_step(self):
+        return 2
+
+
+def time_device(fn, steps, warmup, dist, flush):
+    import torch
+
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0 = time.perf_counter()
+    for a, b in evs:
+        flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall = time.perf_counter() - t0
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return ms, wall
+
+
+def time_e2e(fn, steps, warmup, dist):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        fn()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    return dist.max(wall)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+
+
+def oracle_mha_seconds(wl, repeats=1):
+    import oracle
+
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.mha_fwd(wl.q.f32, wl.k.f32, wl.v.f32, wl.mask_heads, wl.head_map, wl.scale)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, flops, target_s):
+    t1 = oracle_mha_seconds(wl)
+    reps = max(1, int(math.ceil(target_s / max(t1, 1e-3))))
+    t = oracle_mha_seconds(wl, reps) if reps > 1 else t1
+    return {"value": flops * reps / t / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"full {wl.name} workload, {reps} pass(es), fp64 C oracle, {t:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args, dist):
+    """Reference arm: the CPU oracle, as it stands, on the headline workload."""
+    if dist.rank != 0:
+        return
+    wl = mha_workload(args.workload)
+    import oracle
+
+    heads_valid = [oracle.mask_count(m, wl.Lq, wl.Lk) for m in wl.mask_heads]
+    flops = 4.0 * wl.d * valid_pairs(wl, heads_valid)
+    for _ in range(args.warmup):
+        oracle_mha_seconds(wl)
+    times = [oracle_mha_seconds(wl) for _ in range(args.steps)]
+    tot = sum(times)
+    value = flops * args.steps / tot / 1e12
+    line = {"impl": "reference", "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "L": wl.Lq, "d": wl.d},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"full {wl.name} workload per step, fp64 C oracle"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def roofline_obj(bound, achieved, peak, unit, traffic, which):
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": traffic, "peak_source": which}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
+    ap.add_argument("--workload", default="bert-band")
+    ap.add_argument("--extra", default="bigbird,longformer,decode",
+                    help="comma list of secondary workloads (bigbird, longformer, decode) or 'none'")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+        dist.close()
+        return
+
+    import torch
+
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    import split_kv_decode_bsr_gb300 as sta
+
+    sta.lib()  # fails loudly when libsta.so is missing
+    peaks, peak_src = load_peaks()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    # ---- headline: masked MHA on the BERT-base band workload
+    mb = MhaBench(args.workload, dev)
+    with ClockSampler(dist.local) as clk:
+        ms, wall = time_device(mb.step, args.steps, args.warmup, dist, flush)
+    dev_s = dist.max(sum(ms) / 1e3)
+    total_flops = dist.sum(mb.flops * args.steps)
+    value = total_flops / dev_s / 1e12
+    ms_per_step = 1e3 * dev_s / args.steps
+    e2e_s = time_e2e(mb.step_e2e, args.steps, args.warmup, dist)
+    e2e_value = total_flops / e2e_s / 1e12
+    kfile = "mha_block.cu" if mb.kernel == "block" else "mha_row.cu"
+    avg_launch_s = sum(ms) / len(ms) / 1e3
+    achieved = mb.bytes / avg_launch_s / 1e9
+    line = {
+        "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": value, "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": mb.wl.name, "B": mb.wl.B, "H": mb.wl.H, "L": mb.wl.Lq, "d": mb.wl.d,
+                   "mask": "sliding window |i-j|<=64", "valid_pairs": mb.pairs, "kernel": mb.kernel,
+                   "l2": "flushed before every timed launch (256 MiB write)", "parallelism": f"replicas x{dist.world}"},
+        "tensor_frac": (mb.flops / avg_launch_s / 1e12) / peaks["bf16_tflops"],
+        "roofline": roofline_obj("hbm", achieved, peaks["hbm_gbs"], "GB/s", recorded_traffic(kfile, mb.name),
+                                 peak_src),
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": mb.h2d_bytes,
+                "d2h_bytes_per_step": mb.d2h_bytes},
+        "gpu_launches": mb.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    line["roofline"]["algorithmic_bytes_per_launch"] = mb.bytes
+    if dist.rank == 0 and dist.world >= 1:
+        line["cpu_baseline"] = cpu_baseline(mb.wl, mb.flops, args.cpu_seconds) if dist.world == 1 else None
+    del mb
+
+    # ---- secondary workloads
+    extras = {}
+    wanted = [] if args.extra == "none" else [x for x in args.extra.split(",") if x]
+    for name in wanted:
+        steps = max(3, min(args.steps, 10))
+        if name == "decode":
+            db = DecodeBench(dev)
+            ms, _ = time_device(db.step, steps, args.warmup, dist, flush)
+            t = sum(ms) / len(ms) / 1e3
+            gbs = db.kv_bytes / t / 1e9
+            e2e_s = time_e2e(db.step_e2e, steps, args.warmup, dist)
+            extras["decode"] = {
+                "metric": "split-KV decode KV-read GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": 1e3 * t,
+                "config": {"workload": db.wl.name, "T": db.T, "kv_bytes": db.kv_bytes, "num_splits": "auto"},
+                "roofline": roofline_obj("hbm", db.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
+                                         recorded_traffic("decode.cu", "decode"), peak_src),
+                "e2e": {"value": db.kv_bytes / (e2e_s / steps) / 1e9, "unit": "GB/s",
+                        "h2d_bytes_per_step": db.hq.numel() * 2,
+                        "d2h_bytes_per_step": db.ho.numel() * 2 + db.hlse.numel() * 4},
+                "gpu_launches": db.launches_per_step() * steps,
+            }
+            del db
+        else:
+            b = MhaBench(name, dev)
+            ms, _ = time_device(b.step, steps, args.warmup, dist, flush)
+            t = sum(ms) / len(ms) / 1e3
+            tf = b.flops / t / 1e12
+            kf = "mha_block.cu" if b.kernel == "block" else "mha_row.cu"
+            extras[name] = {
+                "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": tf, "unit": "TFLOP/s", "ms_per_step": 1e3 * t,
+                "config": {"workload": b.wl.name, "valid_pairs": b.pairs, "kernel": b.kernel},
+                "tensor_frac": tf / peaks["bf16_tflops"],
+                "roofline": roofline_obj("hbm", b.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
+                                         recorded_traffic(kf, name), peak_src),
+                "gpu_launches": steps,
+            }
+            del b
+        torch.cuda.empty_cache()
+    line["workloads"] = extras
+    err = sta.sta_device_error()
+    if err:
+        line["device_error"] = err
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * sta.h -- C ABI of libsta: masked multi-head attention over a two-level
+ * (BSR + bitmap) mask, and split-KV decode with a log-sum-exp merge, for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations:
+ *  - "Accelerating Sparse Transformer Inference on GPU" (STOF):
+ *      問題定義 -- masked MHA with causal, sliding-window and random masks;
+ *      手法 / 統合 MHA モジュール / 2 段階ストレージ形式 -- outer tiles that are
+ *      empty (skipped), full or part, tracked by pointer arrays, and one uint64
+ *      bitmap per 8x8 inner tile of a part tile;
+ *      デュアルカーネル戦略 / カーネル選択 -- a row-wise kernel for short, highly
+ *      sparse cases, a block-wise kernel for the general case, and an analytic
+ *      model that picks between them.
+ *  - "Cleave: Scaling Tensor Program Optimization via Decoupled Algebraic
+ *    Search and Operator Scheduling": Split演算子によるSplit-Kの対応 and the
+ *    abstract -- a Split operator with split count s parallelises a reduction
+ *    dimension (FlashDecoding); the partial softmax results are merged.
+ *
+ * Conventions (the pages leave these open; plainest readings):
+ *  - Q, K, V, O are [B, H, L, d] row-major, d innermost (decode: Q/O
+ *    [n_req, Hq, d], K/V packed [T, Hkv, d]). LSE is float32, natural log.
+ *  - Mask element 1 = key may be attended (additive 0), 0 = masked (-inf).
+ *  - Outer tiles (OT) are 64x64; inner tiles (IT) 8x8. A part OT stores 64
+ *    uint64 words, ITs row-major (word 8p+q covers OT rows 8p..8p+7, cols
+ *    8q..8q+7); bit 8r+c of a word is element (row r, col c) of its IT.
+ *    An OT is full only if all 4096 elements are in range and valid; edge
+ *    tiles are part with out-of-range bits 0. col_idx is ascending per row.
+ *  - A query row with no valid key yields O = 0 and LSE = -inf.
+ *
+ * Ownership and errors: every pointer to tensor data is a DEVICE pointer
+ * owned by the caller unless marked "host". The library allocates no device
+ * memory, launches only on the given stream (asynchronously) and synchronises
+ * only where a function says so. Arguments are validated on the host before
+ * anything is launched; on error nothing is launched and an sta_status other
+ * than STA_OK is returned (see sta_status_string). STA_ERR_CUDA reports a
+ * launch error from the CUDA runtime.
+ */
+#ifndef STA_H_
+#define STA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int sta_status;
+#define STA_OK 0
+#define STA_ERR_INVALID_ARG 1  /* null pointer, bad size, inconsistent arguments */
+#define STA_ERR_UNSUPPORTED 2  /* dtype / head dim / alignment this build does not handle */
+#define STA_ERR_WORKSPACE 3    /* workspace missing or too small */
+#define STA_ERR_CUDA 4         /* the CUDA runtime reported an error */
+
+typedef int sta_dtype;
+#define STA_BF16 0
+#define STA_F32 1
+
+/* cudaStream_t; NULL is the legacy default stream. */
+typedef void* sta_stream;
+
+/* ------------------------------------------------------------------------ */
+/* Mask sources and the encoded mask                                         */
+/* ------------------------------------------------------------------------ */
+
+#define STA_MASK_PATTERN 0    /* predicate below, no data                     */
+#define STA_MASK_DENSE_U8 1   /* data: uint8 [Lq][Lk], nonzero = valid        */
+#define STA_MASK_DENSE_BITS 2 /* data: uint64 [Lq][ceil(Lk/64)], element (i,j) */
+                              /* at word j>>6, bit j&63; bits j >= Lk ignored  */
+
+/* One [Lq, Lk] mask head. For STA_MASK_PATTERN:
+ *   valid(i,j) = (!causal || j <= i) &&
+ *                ((win_lo <= j-i && j-i <= win_hi) || j < n_global_cols)
+ * which covers causal, sliding-window, banded and global-column masks. */
+typedef struct {
+  int32_t kind;
+  int32_t causal;
+  int64_t win_lo, win_hi;
+  int64_t n_global_cols;
+  const void* data; /* device pointer for the DENSE kinds, else NULL */
+} sta_mask_src;
+
+/* Two-level mask for Hm mask heads (STOF 2 段階ストレージ形式). Row index
+ * of both CSR structures is hm * ot_rows + a (mask head hm, OT row a);
+ * col_idx holds OT column numbers. part_bitmap[t*64 + w] is IT word w of the
+ * t-th part tile. Device arrays are caller-owned; n_* are host copies. */
+typedef struct {
+  int32_t n_mask_heads, Lq, Lk, ot_rows, ot_cols;
+  int32_t* full_row_ptr; /* [Hm*ot_rows + 1] */
+  int32_t* full_col_idx; /* [n_full]         */
+  int32_t* part_row_ptr; /* [Hm*ot_rows + 1] */
+  int32_t* part_col_idx; /* [n_part]         */
+  uint64_t* part_bitmap; /* [n_part * 64]    */
+  int64_t n_full, n_part, n_valid;
+} sta_bsr_mask;
+
+/* sta_encode_mask -- build the two-level mask from Hm sources
+ * (STOF, 2 段階ストレージ形式).
+ *
+ *   srcs            host array [Hm] of mask heads (their data pointers are device)
+ *   Hm, Lq, Lk      mask heads and mask shape, all >= 1, Lq, Lk < 2^30
+ *   out             host struct; see the three modes below
+ *   workspace       device scratch, 256-byte aligned, or NULL
+ *   workspace_bytes host in/out
+ *
+ * Modes:
+ *  1. workspace == NULL: *workspace_bytes is set to the scratch size needed;
+ *     nothing else happens (no CUDA call).
+ *  2. Size query: out->full_row_ptr and out->part_row_ptr set (device,
+ *     [Hm*ot_rows+1] each), out->full_col_idx == out->part_col_idx ==
+ *     out->part_bitmap == NULL. Classifies every outer tile, writes the two
+ *     row_ptr arrays, then SYNCHRONISES the stream and fills out->n_full,
+ *     n_part, n_valid and the shape fields. This is the library's only
+ *     synchronising call.
+ *  3. Fill: all five device arrays set, out->n_full / n_part holding the
+ *     capacities from a size query of the same mask. Writes everything,
+ *     asynchronously. Entries beyond a capacity are never written.
+ * Returns STA_ERR_INVALID_ARG for bad sizes, null pointers or kinds, and
+ * STA_ERR_WORKSPACE if *workspace_bytes is below the requirement. */
+sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, int Lk, sta_bsr_mask* out, void* workspace,
+                           size_t* workspace_bytes, sta_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Masked multi-head attention forward                                       */
+/* ------------------------------------------------------------------------ */
+
+#define STA_KERNEL_AUTO 0  /* analytic selector (STOF カーネル選択)           */
+#define STA_KERNEL_BLOCK 1 /* block-wise: TMA + tcgen05/TMEM, bf16 only        */
+#define STA_KERNEL_ROW 2   /* row-wise: one warp per query row, bf16 or f32   */
+
+/* sta_mha_fwd -- O = softmax(Q K^T * scale + mask) V and its LSE, over the
+ * valid elements of an encoded mask (STOF 問題定義, 統合 MHA モジュール).
+ * Empty outer tiles are skipped, full ones run unmasked, part ones are masked
+ * by their bitmaps.
+ *
+ *   q        [B, H, Lq, d]  dtype        (device)
+ *   k, v     [B, H, Lk, d]  dtype        (device)
+ *   o        [B, H, Lq, d]  dtype        (device, written)
+ *   lse      [B, H, Lq]     float32      (device, written; may be NULL)
+ *   mask     encoded mask with mask->Lq == Lq, mask->Lk == Lk (host struct)
+ *   head_map host [H]: attention head h uses mask head head_map[h]; NULL means
+ *            mask head 0 for every head if Hm == 1, else head h (then Hm must
+ *            equal H)
+ *   d        64 or 128; H <= 1024; B*H <= 65535
+ *   dtype    STA_BF16 (both kernels) or STA_F32 (row-wise kernel only)
+ *   scale    softmax scale, > 0 (e.g. 1/sqrt(d))
+ *   kernel   STA_KERNEL_AUTO / BLOCK / ROW; BLOCK needs bf16 and Lk <= 65536
+ *            (else STA_ERR_UNSUPPORTED)
+ * Pointers must be 16-byte aligned. Asynchronous on `stream`. */
+sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const sta_bsr_mask* mask,
+                       const int32_t* head_map, int B, int H, int Lq, int Lk, int d, sta_dtype dtype, float scale,
+                       int kernel, sta_stream stream);
+
+/* Which kernel sta_mha_fwd would run for these arguments under
+ * STA_KERNEL_AUTO (STA_KERNEL_BLOCK or STA_KERNEL_ROW), or a negative
+ * sta_status on invalid arguments. Host only. */
+int sta_mha_select_kernel(const sta_bsr_mask* mask, int B, int H, int Lq, int Lk, int d, sta_dtype dtype);
+
+/* ------------------------------------------------------------------------ */
+/* Split-KV decode and log-sum-exp merge                                     */
+/* ------------------------------------------------------------------------ */
+
+/* sta_decode_splitkv -- one query token per request against its packed KV
+ * prefix (every key of the request is valid), with the KV reduction split
+ * into chunks that are attended independently and merged by log-sum-exp
+ * (Cleave Split operator; FlashDecoding). GQA: query head h reads kv head
+ * h / (Hq / Hkv).
+ *
+ *   q              [n_req, Hq, d] bf16  (device)
+ *   k, v           [T, Hkv, d]    bf16  (device), request r owns rows
+ *                  kv_indptr[r] .. kv_indptr[r+1]-1; may be NULL when T == 0
+ *                  (every request then gets O = 0, LSE = -inf)
+ *   kv_indptr_dev  int32 [n_req+1] (device), kv_indptr_host: same values (host)
+ *   Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}, d in {64, 128}
+ *   num_splits     0: the library picks the split (the whole token stream is
+ *                  cut into equal ranges, one per resident CTA); s > 0: every
+ *                  request is cut into s chunks of ceil(len/s) keys
+ *   o              [n_req, Hq, d] bf16 (device, written); lse [n_req, Hq] f32
+ *                  (device, written; may be NULL)
+ *   workspace      device scratch for the partial results, 256-byte aligned;
+ *                  workspace == NULL sets *workspace_bytes and returns
+ * kv_indptr_host must be non-decreasing, start at 0, and match the device copy.
+ * Asynchronous on `stream`. */
+sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,
+                              const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d, sta_dtype dtype,
+                              float scale, int num_splits, void* o, float* lse, void* workspace,
+                              size_t* workspace_bytes, sta_stream stream);
+
+/* sta_merge_lse -- merge s partial attention results per row:
+ *   M = max_i lse_i; if M = -inf then O = 0, LSE = -inf; otherwise
+ *   w_i = exp(lse_i - M), O = sum_i w_i O_i / sum_i w_i, LSE = M + log sum_i w_i.
+ *   part_o   [n_rows, s, d] float32 normalised partial outputs (device)
+ *   part_lse [n_rows, s]    float32 natural-log partial denominators (device)
+ *   o        [n_rows, d]    o_dtype (device, written); lse [n_rows] f32 or NULL
+ *   1 <= s <= 4096; d in {32, 64, 128, 256}; n_rows == 0 is a no-op.
+ *   Asynchronous on `stream`. */
+sta_status sta_merge_lse(const float* part_o, const float* part_lse, int n_rows, int s, int d, void* o,
+                         sta_dtype o_dtype, float* lse, sta_stream stream);
+
+/* Static string describing a status code. */
+const char* sta_status_string(sta_status status);
+
+/* Device error word of the current device: kernels whose internal waits
+ * (mbarrier phases, bounded to about 2 s) give up record a nonzero code here
+ * instead of hanging; 0 means no such event. Copies the word to *code
+ * (synchronous) and clears it when reset != 0. */
+sta_status sta_device_error(int* code, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STA_H_ */

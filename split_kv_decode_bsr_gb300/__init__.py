@@ -1,0 +1,311 @@
+"""Python binding of libsta (masked MHA over a two-level BSR + bitmap mask, split-KV decode).
+
+Thin ctypes marshalling over the C ABI in ``include/sta.h``: every function of the
+same name calls the CUDA library, on the current torch stream, with device memory
+held in torch tensors. There is no fallback: when ``libsta.so`` has not been built
+(``python -m split_kv_decode_bsr_gb300.build`` or ``__graft_entry__.build()``) every
+call raises.
+
+Operations (sources):
+  * ``sta_encode_mask`` -- STOF's two-level storage format ("Accelerating Sparse
+    Transformer Inference on GPU", 手法 / 2 段階ストレージ形式).
+  * ``sta_mha_fwd`` -- masked MHA forward with the row-wise / block-wise kernels and
+    the analytic selector (same page, デュアルカーネル戦略 / カーネル選択).
+  * ``sta_decode_splitkv`` / ``sta_merge_lse`` -- Cleave's Split operator on the KV
+    reduction of GQA decode with a log-sum-exp merge ("Cleave: Scaling Tensor
+    Program Optimization ...", Split演算子によるSplit-Kの対応).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+import threading
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsta.so")
+
+STA_OK, STA_ERR_INVALID_ARG, STA_ERR_UNSUPPORTED, STA_ERR_WORKSPACE, STA_ERR_CUDA = 0, 1, 2, 3, 4
+STA_BF16, STA_F32 = 0, 1
+STA_MASK_PATTERN, STA_MASK_DENSE_U8, STA_MASK_DENSE_BITS = 0, 1, 2
+STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
+_KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
+
+EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_select_kernel", "sta_decode_splitkv", "sta_merge_lse",
+            "sta_status_string", "sta_device_error")
+
+BIG = 1 << 40
+
+
+class StaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+class _MaskSrc(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("causal", C.c_int32), ("win_lo", C.c_int64), ("win_hi", C.c_int64),
+                ("n_global_cols", C.c_int64), ("data", C.c_void_p)]
+
+
+class _BsrMask(C.Structure):
+    _fields_ = [("n_mask_heads", C.c_int32), ("Lq", C.c_int32), ("Lk", C.c_int32), ("ot_rows", C.c_int32),
+                ("ot_cols", C.c_int32), ("full_row_ptr", C.c_void_p), ("full_col_idx", C.c_void_p),
+                ("part_row_ptr", C.c_void_p), ("part_col_idx", C.c_void_p), ("part_bitmap", C.c_void_p),
+                ("n_full", C.c_int64), ("n_part", C.c_int64), ("n_valid", C.c_int64)]
+
+
+_lock = threading.Lock()
+_lib_handle = None
+
+
+def lib():
+    """The loaded libsta.so (raises if it has not been built)."""
+    global _lib_handle
+    with _lock:
+        if _lib_handle is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libsta.so not built at {LIB_PATH}; run split_kv_decode_bsr_gb300.build.build()")
+            h = C.CDLL(LIB_PATH)
+            P, i32, f32, sz = C.c_void_p, C.c_int, C.c_float, C.POINTER(C.c_size_t)
+            h.sta_encode_mask.argtypes = [P, i32, i32, i32, C.POINTER(_BsrMask), P, sz, P]
+            h.sta_mha_fwd.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32, i32, P]
+            h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
+            h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
+            h.sta_merge_lse.argtypes = [P, P, i32, i32, i32, P, i32, P, P]
+            h.sta_status_string.argtypes = [i32]
+            h.sta_status_string.restype = C.c_char_p
+            h.sta_device_error.argtypes = [C.POINTER(C.c_int), i32]
+            for n in EXPORTED:
+                if n not in ("sta_status_string",):
+                    getattr(h, n).restype = C.c_int
+            _lib_handle = h
+    return _lib_handle
+
+
+def status_string(status: int) -> str:
+    return lib().sta_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != STA_OK:
+        raise StaError(fn, status)
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return STA_BF16
+    if dt == torch.float32:
+        return STA_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+# ---------------------------------------------------------------------------
+# mask sources and the encoded mask
+
+
+@dataclass
+class MaskSource:
+    """One [Lq, Lk] mask head: a pattern, or dense uint8 / bit-packed device data.
+
+    Pattern: valid(i, j) = (not causal or j <= i) and
+                           (win_lo <= j - i <= win_hi or j < n_global_cols).
+    Bits: int64/uint64 tensor [Lq, ceil(Lk/64)], element (i, j) at word j >> 6, bit j & 63.
+    """
+    kind: int
+    causal: int = 0
+    win_lo: int = -BIG
+    win_hi: int = BIG
+    n_global_cols: int = 0
+    data: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def pattern(causal=False, win_lo=-BIG, win_hi=BIG, n_global_cols=0) -> "MaskSource":
+        return MaskSource(STA_MASK_PATTERN, int(bool(causal)), int(win_lo), int(win_hi), int(n_global_cols))
+
+    @staticmethod
+    def dense_u8(t: torch.Tensor) -> "MaskSource":
+        assert t.is_cuda and t.dtype == torch.uint8 and t.dim() == 2 and t.is_contiguous()
+        return MaskSource(STA_MASK_DENSE_U8, data=t)
+
+    @staticmethod
+    def dense_bits(t: torch.Tensor) -> "MaskSource":
+        assert t.is_cuda and t.dtype in (torch.int64, torch.uint64) and t.dim() == 2 and t.is_contiguous()
+        return MaskSource(STA_MASK_DENSE_BITS, data=t)
+
+
+class BsrMask:
+    """Encoded two-level mask: device tensors plus host counts (mirrors sta_bsr_mask)."""
+
+    def __init__(self, Hm, Lq, Lk, full_row_ptr, full_col_idx, part_row_ptr, part_col_idx, part_bitmap,
+                 n_full, n_part, n_valid):
+        self.Hm, self.Lq, self.Lk = Hm, Lq, Lk
+        self.ot_rows, self.ot_cols = (Lq + 63) // 64, (Lk + 63) // 64
+        self.full_row_ptr, self.full_col_idx = full_row_ptr, full_col_idx
+        self.part_row_ptr, self.part_col_idx = part_row_ptr, part_col_idx
+        self.part_bitmap = part_bitmap
+        self.n_full, self.n_part, self.n_valid = n_full, n_part, n_valid
+
+    def struct(self) -> _BsrMask:
+        s = _BsrMask()
+        s.n_mask_heads, s.Lq, s.Lk, s.ot_rows, s.ot_cols = self.Hm, self.Lq, self.Lk, self.ot_rows, self.ot_cols
+        s.full_row_ptr = self.full_row_ptr.data_ptr()
+        s.full_col_idx = self.full_col_idx.data_ptr() if self.n_full else None
+        s.part_row_ptr = self.part_row_ptr.data_ptr()
+        s.part_col_idx = self.part_col_idx.data_ptr() if self.n_part else None
+        s.part_bitmap = self.part_bitmap.data_ptr() if self.n_part else None
+        s.n_full, s.n_part, s.n_valid = self.n_full, self.n_part, self.n_valid
+        return s
+
+    def host_arrays(self) -> dict:
+        return dict(full_row_ptr=self.full_row_ptr.cpu().numpy(), full_col_idx=self.full_col_idx.cpu().numpy(),
+                    part_row_ptr=self.part_row_ptr.cpu().numpy(), part_col_idx=self.part_col_idx.cpu().numpy(),
+                    part_bitmap=self.part_bitmap.cpu().numpy().view("uint64").reshape(-1, 64),
+                    n_full=self.n_full, n_part=self.n_part, n_valid=self.n_valid)
+
+
+def _src_array(srcs: Sequence[MaskSource]):
+    arr = (_MaskSrc * len(srcs))()
+    for i, s in enumerate(srcs):
+        arr[i].kind, arr[i].causal, arr[i].win_lo, arr[i].win_hi = s.kind, s.causal, s.win_lo, s.win_hi
+        arr[i].n_global_cols = s.n_global_cols
+        arr[i].data = s.data.data_ptr() if s.data is not None else None
+    return arr
+
+
+def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, stream=None) -> BsrMask:
+    """Encode Hm = len(srcs) mask heads (size query, then fill). Synchronises once."""
+    h = lib()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    Hm = len(srcs)
+    arr = _src_array(srcs)
+    ws_bytes = C.c_size_t(0)
+    out = _BsrMask()
+    _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), None, C.byref(ws_bytes), None))
+    ws = torch.empty(max(int(ws_bytes.value), 256), dtype=torch.uint8, device=dev)
+    R = (Lq + 63) // 64
+    frp = torch.empty(Hm * R + 1, dtype=torch.int32, device=dev)
+    prp = torch.empty(Hm * R + 1, dtype=torch.int32, device=dev)
+    out.full_row_ptr, out.part_row_ptr = frp.data_ptr(), prp.data_ptr()
+    st = _stream(stream)
+    _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
+    nf, npart, nv = int(out.n_full), int(out.n_part), int(out.n_valid)
+    fci = torch.empty(max(nf, 1), dtype=torch.int32, device=dev)
+    pci = torch.empty(max(npart, 1), dtype=torch.int32, device=dev)
+    pbm = torch.empty(max(npart, 1) * 64, dtype=torch.int64, device=dev)
+    out.full_col_idx, out.part_col_idx, out.part_bitmap = fci.data_ptr(), pci.data_ptr(), pbm.data_ptr()
+    _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
+    return BsrMask(Hm, Lq, Lk, frp, fci[:nf], prp, pci[:npart], pbm[:npart * 64], nf, npart, nv)
+
+
+# ---------------------------------------------------------------------------
+# masked MHA
+
+
+def sta_mha_select_kernel(mask: BsrMask, B: int, H: int, d: int, dtype=torch.bfloat16) -> str:
+    s = mask.struct()
+    r = lib().sta_mha_select_kernel(C.byref(s), B, H, mask.Lq, mask.Lk, d, _dtype_code(dtype))
+    if r < 0:
+        raise StaError("sta_mha_select_kernel", -r)
+    return {STA_KERNEL_BLOCK: "block", STA_KERNEL_ROW: "row"}[r]
+
+
+def sta_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BsrMask, head_map=None, scale=None,
+                kernel: str = "auto", o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                stream=None):
+    """O = softmax(Q K^T * scale + mask) V and LSE; q [B,H,Lq,d], k/v [B,H,Lk,d] (bf16 or fp32)."""
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous()
+    assert k.shape == (B, H, Lk, d) and v.shape == k.shape and q.dtype == k.dtype == v.dtype
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    hm = None
+    if head_map is not None:
+        hm = (C.c_int32 * H)(*[int(x) for x in head_map])
+    s = mask.struct()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().sta_mha_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), C.byref(s), hm, B, H, Lq, Lk, d,
+                           _dtype_code(q.dtype), scale, _KERNELS[kernel], _stream(stream))
+    _check("sta_mha_fwd", st)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# split-KV decode and merge
+
+
+def _indptr_host(kv_indptr) -> "C.Array":
+    vals = kv_indptr.tolist() if hasattr(kv_indptr, "tolist") else list(kv_indptr)
+    return (C.c_int32 * len(vals))(*[int(x) for x in vals])
+
+
+def decode_workspace_bytes(kv_indptr, n_req, Hq, Hkv, d, num_splits=0) -> int:
+    n = C.c_size_t(0)
+    ind = _indptr_host(kv_indptr)
+    _check("sta_decode_splitkv", lib().sta_decode_splitkv(None, None, None, None, ind, n_req, Hq, Hkv, d, STA_BF16,
+                                                           1.0, num_splits, None, None, None, C.byref(n), None))
+    return int(n.value)
+
+
+def sta_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_indptr_dev: torch.Tensor, kv_indptr_host,
+                       scale=None, num_splits: int = 0, o=None, lse=None, workspace=None, stream=None):
+    """GQA decode: q [n_req, Hq, d], k/v [T, Hkv, d] bf16, kv_indptr int32 [n_req + 1]."""
+    n_req, Hq, d = q.shape
+    T, Hkv, dk = k.shape
+    assert dk == d and v.shape == k.shape and kv_indptr_dev.dtype == torch.int32
+    ind = _indptr_host(kv_indptr_host)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((n_req, Hq), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = C.c_size_t(0)
+    h = lib()
+    _check("sta_decode_splitkv", h.sta_decode_splitkv(None, None, None, None, ind, n_req, Hq, Hkv, d,
+                                                       _dtype_code(q.dtype), scale, num_splits, None, None, None,
+                                                       C.byref(need), None))
+    if workspace is None or workspace.numel() < need.value:
+        workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=q.device)
+    have = C.c_size_t(workspace.numel())
+    _check("sta_decode_splitkv", h.sta_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr_dev), ind, n_req, Hq,
+                                                       Hkv, d, _dtype_code(q.dtype), scale, num_splits, _ptr(o),
+                                                       _ptr(lse), _ptr(workspace), C.byref(have), _stream(stream)))
+    return o, lse
+
+
+def sta_merge_lse(part_o: torch.Tensor, part_lse: torch.Tensor, o_dtype=torch.bfloat16, o=None, lse=None,
+                  stream=None):
+    """Merge partials: part_o [n_rows, s, d] fp32, part_lse [n_rows, s] fp32 -> o [n_rows, d], lse [n_rows]."""
+    n_rows, s, d = part_o.shape
+    assert part_o.dtype == torch.float32 and part_lse.shape == (n_rows, s) and part_lse.dtype == torch.float32
+    if o is None:
+        o = torch.empty((n_rows, d), dtype=o_dtype, device=part_o.device)
+    if lse is None:
+        lse = torch.empty((n_rows,), dtype=torch.float32, device=part_o.device)
+    _check("sta_merge_lse", lib().sta_merge_lse(_ptr(part_o.contiguous()), _ptr(part_lse.contiguous()), n_rows, s, d,
+                                                _ptr(o), _dtype_code(o.dtype), _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+def sta_device_error(reset: bool = True) -> int:
+    code = C.c_int(0)
+    _check("sta_device_error", lib().sta_device_error(C.byref(code), int(reset)))
+    return int(code.value)

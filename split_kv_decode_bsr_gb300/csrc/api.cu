@@ -1,0 +1,194 @@
+// C-ABI entry points of libsta: host-side validation, the analytic kernel
+// selector, the split planner, and the launches (all on the caller's stream).
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+
+namespace sta {
+
+// Device error word written by bounded waits that time out (first code wins).
+__device__ int g_dev_error = 0;
+
+int* device_error_word() {
+  static int* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int*>(p);
+  }
+  return cached[dev];
+}
+
+namespace {
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Analytic selector (STOF カーネル選択: mask sparsity and sequence length decide
+// between the row-wise and the block-wise kernel). Cost model, per query head:
+//   block: every non-empty outer tile costs a 128x64 tile pair of MMAs plus the
+//          softmax of 64x64 scores;   t_b = (n_full + n_part) * 4096 * kBlockPair
+//   row:   every valid (q, k) pair costs 4*d FMA-pipe flops plus a gather;
+//          t_r = n_valid * d * kRowPair
+// with a fixed per-launch cost added to the block kernel. The constants are
+// calibrated on GB300 by the bench's selector sweep.
+constexpr double kBlockPairPerD = 1.0 / 64.0;  // relative cost of one computed pair per unit d (block)
+constexpr double kRowPairPerD = 1.0 / 2.0;     // relative cost of one valid pair per unit d (row)
+
+int select_kernel(const sta_bsr_mask* m, int d, int Lk, sta_dtype dtype) {
+  if (dtype != STA_BF16 || !block_kernel_supports(d, Lk, dtype)) return STA_KERNEL_ROW;
+  const double computed = (double)(m->n_full + m->n_part) * 4096.0;
+  const double t_block = computed * d * kBlockPairPerD;
+  const double t_row = (double)m->n_valid * d * kRowPairPerD;
+  return t_row < t_block ? STA_KERNEL_ROW : STA_KERNEL_BLOCK;
+}
+
+sta_status check_mask(const sta_bsr_mask* mask, int Lq, int Lk) {
+  if (!mask) return STA_ERR_INVALID_ARG;
+  if (mask->Lq != Lq || mask->Lk != Lk || mask->n_mask_heads < 1) return STA_ERR_INVALID_ARG;
+  if (mask->ot_rows != (int)cdiv(Lq, 64) || mask->ot_cols != (int)cdiv(Lk, 64)) return STA_ERR_INVALID_ARG;
+  if (!mask->full_row_ptr || !mask->part_row_ptr) return STA_ERR_INVALID_ARG;
+  if ((mask->n_full > 0 && !mask->full_col_idx) || (mask->n_part > 0 && (!mask->part_col_idx || !mask->part_bitmap)))
+    return STA_ERR_INVALID_ARG;
+  return STA_OK;
+}
+
+}  // namespace
+}  // namespace sta
+
+using namespace sta;
+
+extern "C" const char* sta_status_string(sta_status s) {
+  switch (s) {
+    case STA_OK: return "ok";
+    case STA_ERR_INVALID_ARG: return "invalid argument";
+    case STA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case STA_ERR_WORKSPACE: return "workspace missing or too small";
+    case STA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+extern "C" sta_status sta_device_error(int* code, int reset) {
+  if (!code) return STA_ERR_INVALID_ARG;
+  int* w = device_error_word();
+  if (!w) return STA_ERR_CUDA;
+  STA_CUDA_TRY(cudaMemcpy(code, w, sizeof(int), cudaMemcpyDeviceToHost));
+  if (reset) STA_CUDA_TRY(cudaMemset(w, 0, sizeof(int)));
+  return STA_OK;
+}
+
+extern "C" int sta_mha_select_kernel(const sta_bsr_mask* mask, int B, int H, int Lq, int Lk, int d, sta_dtype dtype) {
+  if (B < 1 || H < 1 || (d != 64 && d != 128) || (dtype != STA_BF16 && dtype != STA_F32)) return -STA_ERR_INVALID_ARG;
+  const sta_status st = check_mask(mask, Lq, Lk);
+  if (st != STA_OK) return -st;
+  return select_kernel(mask, d, Lk, dtype);
+}
+
+extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq, int Lk,
+                                  int d, sta_dtype dtype, float scale, int kernel, sta_stream stream) {
+  if (!q || !k || !v || !o) return STA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || H > kMaxHeads || (int64_t)B * H > 65535) return STA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return STA_ERR_INVALID_ARG;
+  if (dtype != STA_BF16 && dtype != STA_F32) return STA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return STA_ERR_UNSUPPORTED;
+  if (kernel < STA_KERNEL_AUTO || kernel > STA_KERNEL_ROW) return STA_ERR_INVALID_ARG;
+  sta_status st = check_mask(mask, Lq, Lk);
+  if (st != STA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return STA_ERR_UNSUPPORTED;
+  if (lse && ((uintptr_t)lse & 3u)) return STA_ERR_UNSUPPORTED;
+  MhaArgs a;
+  memset(&a, 0, sizeof(a));
+  const int Hm = mask->n_mask_heads;
+  for (int h = 0; h < H; ++h) {
+    int mh;
+    if (head_map) mh = head_map[h];
+    else if (Hm == 1) mh = 0;
+    else if (Hm == H) mh = h;
+    else return STA_ERR_INVALID_ARG;
+    if (mh < 0 || mh >= Hm) return STA_ERR_INVALID_ARG;
+    a.hmap.m[h] = (uint16_t)mh;
+  }
+  int which = kernel == STA_KERNEL_AUTO ? select_kernel(mask, d, Lk, dtype) : kernel;
+  if (which == STA_KERNEL_BLOCK && !block_kernel_supports(d, Lk, dtype)) return STA_ERR_UNSUPPORTED;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.mask = MaskView{mask->full_row_ptr, mask->full_col_idx, mask->part_row_ptr, mask->part_col_idx,
+                    mask->part_bitmap, mask->ot_rows, mask->ot_cols};
+  a.B = B; a.H = H; a.Lq = Lq; a.Lk = Lk; a.d = d; a.dtype = dtype;
+  a.scale_log2 = scale * kLog2e;
+  a.err = device_error_word();
+  cudaStream_t s = (cudaStream_t)stream;
+  return which == STA_KERNEL_BLOCK ? launch_mha_block(a, s) : launch_mha_row(a, s);
+}
+
+namespace {
+
+sta_status decode_setup(const int32_t* indptr_host, int n_req, int Hq, int Hkv, int d, sta_dtype dtype, int num_splits,
+                        DecodeArgs& a, int64_t& T) {
+  if (!indptr_host || n_req < 1 || Hq < 1 || Hkv < 1 || num_splits < 0 || num_splits > 4096)
+    return STA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return STA_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return STA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return STA_ERR_UNSUPPORTED;
+  if (dtype != STA_BF16) return STA_ERR_UNSUPPORTED;
+  if (indptr_host[0] != 0) return STA_ERR_INVALID_ARG;
+  for (int r = 0; r < n_req; ++r)
+    if (indptr_host[r + 1] < indptr_host[r]) return STA_ERR_INVALID_ARG;
+  T = indptr_host[n_req];
+  if ((int64_t)n_req * Hq > INT32_MAX / 2) return STA_ERR_INVALID_ARG;
+  memset(&a, 0, sizeof(a));
+  a.n_req = n_req; a.Hq = Hq; a.Hkv = Hkv; a.d = d;
+  a.mode = num_splits == 0 ? 0 : 1;
+  a.splits = num_splits;
+  int dev = 0;
+  STA_CUDA_TRY(cudaGetDevice(&dev));
+  return decode_plan(a, T, dev);
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,
+                                         const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d,
+                                         sta_dtype dtype, float scale, int num_splits, void* o, float* lse,
+                                         void* workspace, size_t* workspace_bytes, sta_stream stream) {
+  if (!workspace_bytes) return STA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return STA_ERR_INVALID_ARG;
+  DecodeArgs a;
+  int64_t T = 0;
+  sta_status st = decode_setup(kv_indptr_host, n_req, Hq, Hkv, d, dtype, num_splits, a, T);
+  if (st != STA_OK) return st;
+  const size_t slots = decode_slots(a);
+  const size_t o_bytes = align256(slots * (size_t)Hq * d * sizeof(float));
+  const size_t need = o_bytes + align256(slots * (size_t)Hq * sizeof(float));
+  if (!workspace) {
+    *workspace_bytes = need;
+    return STA_OK;
+  }
+  if (*workspace_bytes < need) return STA_ERR_WORKSPACE;
+  if (!q || !kv_indptr_dev || !o) return STA_ERR_INVALID_ARG;
+  if (T > 0 && (!k || !v)) return STA_ERR_INVALID_ARG;  // K/V may be empty (NULL) only when T == 0
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)workspace & 255u))
+    return STA_ERR_UNSUPPORTED;
+  a.q = q; a.k = k; a.v = v; a.kv_indptr = kv_indptr_dev; a.o = o; a.lse = lse;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  a.scale_log2 = scale * kLog2e;
+  a.err = device_error_word();
+  return launch_decode(a, (cudaStream_t)stream);
+}
+
+extern "C" sta_status sta_merge_lse(const float* part_o, const float* part_lse, int n_rows, int s, int d, void* o,
+                                    sta_dtype o_dtype, float* lse, sta_stream stream) {
+  if (n_rows < 0 || s < 1 || s > 4096) return STA_ERR_INVALID_ARG;
+  if (o_dtype != STA_BF16 && o_dtype != STA_F32) return STA_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return STA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return STA_OK;
+  if (!part_o || !part_lse || !o) return STA_ERR_INVALID_ARG;
+  return launch_merge_public(part_o, part_lse, n_rows, s, d, o, o_dtype, lse, (cudaStream_t)stream);
+}

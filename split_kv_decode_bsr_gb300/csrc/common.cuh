@@ -1,0 +1,67 @@
+// Shared device/host helpers of libsta (CUDA path only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sta.h"
+
+#define STA_OT 64  // outer tile edge
+#define STA_IT 8   // inner tile edge
+
+namespace sta {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// bf16 <-> f32 without library conversions on the hot path: widening is exact.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Device copy of the encoded-mask arrays a kernel needs.
+struct MaskView {
+  const int32_t* full_row_ptr;
+  const int32_t* full_col_idx;
+  const int32_t* part_row_ptr;
+  const int32_t* part_col_idx;
+  const uint64_t* part_bitmap;
+  int32_t ot_rows, ot_cols;
+};
+
+// Row r (0..63) of a part outer tile: 64-bit key mask, bit c = column c of the tile.
+// Byte (r % 8) of IT word 8*(r/8) + q holds columns 8q..8q+7 of that row.
+__device__ __forceinline__ uint64_t part_row_bits(const uint64_t* words, int r) {
+  const int p = r >> 3, sh = (r & 7) * 8;
+  uint64_t m = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) m |= ((words[8 * p + q] >> sh) & 0xFFull) << (8 * q);
+  return m;
+}
+
+}  // namespace sta
+
+#define STA_CUDA_TRY(expr)                          \
+  do {                                              \
+    cudaError_t e_ = (expr);                        \
+    if (e_ != cudaSuccess) return STA_ERR_CUDA;     \
+  } while (0)
+
+#define STA_LAUNCH_CHECK()                          \
+  do {                                              \
+    cudaError_t e_ = cudaGetLastError();            \
+    if (e_ != cudaSuccess) return STA_ERR_CUDA;     \
+  } while (0)

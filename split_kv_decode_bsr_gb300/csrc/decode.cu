@@ -1,0 +1,484 @@
+// Split-KV GQA decode and log-sum-exp merge (Cleave, Split演算子によるSplit-Kの対応:
+// a Split operator with a split count s parallelises the KV reduction; each
+// chunk is attended on its own and the partial softmax results are merged).
+//
+// Decode kernel: persistent-style CTAs, each owning a list of KV segments
+// (request r, token range [a, b)) and a block of HB kv heads. One producer warp
+// streams K/V tiles (NT tokens x HB heads x d, bf16) from HBM into a ring of
+// shared-memory stages with 1-D bulk copies completing on mbarriers; HB consumer
+// warps (one per kv head) score the G query heads of their group against each
+// tile on the FMA pipe (lanes own d/32 dimensions; a 32-way reduce-scatter over
+// shuffles turns per-lane partial dot products into one full score per lane),
+// run an fp32 online softmax per query head, and accumulate P.V. A segment that
+// covers its whole request writes O (bf16) and LSE directly; otherwise it writes
+// a normalised fp32 partial and its LSE, merged afterwards.
+//
+// Split plans: mode 0 cuts the concatenated token stream [0, T) into equal
+// ranges, one per CTA (balanced work whatever the length mix; partial slot of
+// (CTA x, request r) = x + r, unique because both grow along the stream);
+// mode 1 cuts every request into s chunks of ceil(len / s) keys (slot r*s + c).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sta {
+namespace {
+
+enum : int { kFirst = 1, kLast = 2, kFinal = 4, kDone = 8 };
+
+struct StageInfo {
+  int r, tok0, n, flags, slot;
+};
+
+template <int G, int D, int HB>
+struct DecCfg {
+  static constexpr int E = D / 32;
+  static constexpr int TG = 32 / G;             // tokens per reduce-scatter group
+  static constexpr int NT = TG > 8 ? TG : 8;    // tokens per tile
+  static constexpr int GROUPS = NT / TG;
+  static constexpr int TILE_BYTES = NT * HB * D * 2;  // K or V part of one stage
+  static constexpr int STAGES_RAW = 196608 / (2 * TILE_BYTES);
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
+  static constexpr int SMEM = STAGES * 2 * TILE_BYTES;
+  static constexpr int THREADS = (HB + 1) * 32;
+};
+
+// Largest r with indptr[r] <= t (indptr non-decreasing, indptr[0] = 0 <= t).
+__device__ __forceinline__ int find_request(const int32_t* indptr, int n_req, int t) {
+  int lo = 0, hi = n_req;  // answer in [0, n_req]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(indptr + mid) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int G, int D, int HB>
+__global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const DecodeArgs A) {
+  using Cfg = DecCfg<G, D, HB>;
+  constexpr int E = Cfg::E, TG = Cfg::TG, NT = Cfg::NT, STAGES = Cfg::STAGES;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ StageInfo info[STAGES];
+  __shared__ __align__(16) float s_p[HB][TG * G];
+  __shared__ float s_alpha[HB][G];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g0 = blockIdx.y * HB;  // first kv head of this CTA
+  const int Hkv = A.Hkv;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], HB);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == HB) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    auto emit = [&](int r, int a, int n, int flags, int slot) -> bool {
+      if (lane == 0) ok = mbar_wait(&empty_bar[stage], (round & 1u) ^ 1u, A.err, 0x101);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return false;
+      if (lane == 0) {
+        info[stage] = StageInfo{r, a, n, flags, slot};
+        if (n > 0) mbar_arrive_expect_tx(&full_bar[stage], (uint32_t)(2 * n * HB * D * 2));
+        else mbar_arrive(&full_bar[stage]);
+      }
+      __syncwarp();
+      if (n > 0) {
+        uint8_t* ks = smem + (size_t)stage * 2 * Cfg::TILE_BYTES;
+        uint8_t* vs = ks + Cfg::TILE_BYTES;
+        const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(A.k);
+        const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(A.v);
+        if (HB == Hkv) {
+          if (lane == 0) {
+            const size_t off = (size_t)a * Hkv * D;
+            bulk_g2s(ks, kg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
+            bulk_g2s(vs, vg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
+          }
+        } else if (lane < n) {
+          const size_t off = ((size_t)(a + lane) * Hkv + g0) * D;
+          bulk_g2s(ks + lane * HB * D * 2, kg + off, HB * D * 2, &full_bar[stage]);
+          bulk_g2s(vs + lane * HB * D * 2, vg + off, HB * D * 2, &full_bar[stage]);
+        }
+      }
+      if (++stage == STAGES) { stage = 0; ++round; }
+      return true;
+    };
+    auto emit_segment = [&](int r, int a, int b, bool final, int slot) -> bool {
+      if (a >= b) return emit(r, a, 0, kFirst | kLast | (final ? kFinal : 0), slot);
+      for (int t = a; t < b; t += NT) {
+        const int n = min(NT, b - t);
+        const int flags = (t == a ? kFirst : 0) | (t + NT >= b ? kLast : 0) | (final ? kFinal : 0);
+        if (!emit(r, t, n, flags, slot)) return false;
+      }
+      return true;
+    };
+    if (A.mode == 0) {
+      const int T = __ldg(A.kv_indptr + A.n_req);
+      const int start = blockIdx.x * A.range_len;
+      const int end = min(T, start + A.range_len);
+      if (start < end) {
+        int r = find_request(A.kv_indptr, A.n_req, start);
+        int a = start;
+        while (a < end && r < A.n_req) {
+          const int rb = __ldg(A.kv_indptr + r), re = __ldg(A.kv_indptr + r + 1);
+          if (re <= a) { ++r; continue; }
+          const int b = min(end, re);
+          if (!emit_segment(r, a, b, a == rb && b == re, blockIdx.x + r)) break;
+          a = b;
+          ++r;
+        }
+      }
+    } else {
+      const int s = A.splits;
+      for (int it = blockIdx.x; it < A.n_req * s; it += gridDim.x) {
+        const int r = it / s, c = it % s;
+        const int rb = __ldg(A.kv_indptr + r), len = __ldg(A.kv_indptr + r + 1) - rb;
+        const int cl = (len + s - 1) / s;
+        const int a = rb + min(len, c * cl), b = rb + min(len, (c + 1) * cl);
+        if (!emit_segment(r, a, b, s == 1, it)) break;
+      }
+    }
+    emit(0, 0, 0, kDone, 0);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = g0 + warp;  // kv head of this warp
+  const int Hq = A.Hq;
+  float q[G][E], acc[G][E];
+  float m_l = -INFINITY, l_l = 0.f;  // running max / sum of head (lane / TG)
+  int stage = 0;
+  uint32_t round = 0;
+  const int my_h = lane / TG, my_t = lane % TG;
+  for (;;) {
+    if (!mbar_wait(&full_bar[stage], round & 1u, A.err, 0x102)) break;
+    const StageInfo inf = info[stage];
+    if (inf.flags & kDone) break;
+    if (inf.flags & kFirst) {
+      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(A.q) + ((size_t)inf.r * Hq + (size_t)g * G) * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qg + h * D + lane * E + e));
+          q[h][e] = bf16lo(w) * A.scale_log2;
+          q[h][e + 1] = bf16hi(w) * A.scale_log2;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+      }
+      m_l = -INFINITY;
+      l_l = 0.f;
+    }
+    const __nv_bfloat16* ks =
+        reinterpret_cast<const __nv_bfloat16*>(smem + (size_t)stage * 2 * Cfg::TILE_BYTES) + warp * D + lane * E;
+    const __nv_bfloat16* vs = ks + Cfg::TILE_BYTES / 2;
+#pragma unroll 1
+    for (int grp = 0; grp < Cfg::GROUPS; ++grp) {
+      const int tb = grp * TG;
+      if (tb >= inf.n) break;
+      float vals[32];
+#pragma unroll
+      for (int t = 0; t < TG; ++t) {
+        float kf[E];
+        const __nv_bfloat16* kp = ks + (size_t)(tb + t) * HB * D;
+        if constexpr (E == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(kp);
+          kf[0] = bf16lo(w.x); kf[1] = bf16hi(w.x); kf[2] = bf16lo(w.y); kf[3] = bf16hi(w.y);
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(kp);
+          kf[0] = bf16lo(w); kf[1] = bf16hi(w);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float x = q[h][0] * kf[0];
+#pragma unroll
+          for (int e = 1; e < E; ++e) x = fmaf(q[h][e], kf[e], x);
+          vals[h * TG + t] = x;
+        }
+      }
+      // 32-way reduce-scatter: afterwards lane holds the full score of value `lane`.
+#pragma unroll
+      for (int k = 16; k >= 1; k >>= 1) {
+        const bool upper = (lane & k) != 0;
+#pragma unroll
+        for (int i = 0; i < k; ++i) {
+          const float send = upper ? vals[i] : vals[i + k];
+          const float keep = upper ? vals[i + k] : vals[i];
+          vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+        }
+      }
+      const bool valid = tb + my_t < inf.n;
+      const float s = valid ? vals[0] : -INFINITY;
+      float mx = s;
+#pragma unroll
+      for (int o = TG / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m_l, mx);
+      const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_l - m_new);
+      const float p = valid ? exp2f(s - m_new) : 0.f;
+      float ps = p;
+#pragma unroll
+      for (int o = TG / 2; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l_l = l_l * alpha + ps;
+      m_l = m_new;
+      s_p[warp][my_t * G + my_h] = p;
+      if (my_t == 0) s_alpha[warp][my_h] = alpha;
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float a_h = s_alpha[warp][h];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[h][e] *= a_h;
+      }
+      const int nv = min(TG, inf.n - tb);
+#pragma unroll 4
+      for (int t = 0; t < nv; ++t) {
+        float pv[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) pv[h] = s_p[warp][t * G + h];
+        float vf[E];
+        const __nv_bfloat16* vp = vs + (size_t)(tb + t) * HB * D;
+        if constexpr (E == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(vp);
+          vf[0] = bf16lo(w.x); vf[1] = bf16hi(w.x); vf[2] = bf16lo(w.y); vf[3] = bf16hi(w.y);
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
+          vf[0] = bf16lo(w); vf[1] = bf16hi(w);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pv[h], vf[e], acc[h][e]);
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[stage]);
+    if (++stage == STAGES) { stage = 0; ++round; }
+
+    if (inf.flags & kLast) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float l_h = __shfl_sync(0xffffffffu, l_l, h * TG);
+        const float m_h = __shfl_sync(0xffffffffu, m_l, h * TG);
+        const float inv = l_h > 0.f ? 1.f / l_h : 0.f;
+        const float lse_h = l_h > 0.f ? (m_h + log2f(l_h)) * kLn2 : -INFINITY;
+        const size_t row = (size_t)g * G + h;
+        if (inf.flags & kFinal) {
+          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + ((size_t)inf.r * Hq + row) * D + lane * E;
+#pragma unroll
+          for (int e = 0; e < E; e += 2)
+            *reinterpret_cast<__nv_bfloat162*>(op + e) = __floats2bfloat162_rn(acc[h][e] * inv, acc[h][e + 1] * inv);
+          if (A.lse && lane == 0) A.lse[(size_t)inf.r * Hq + row] = lse_h;
+        } else {
+          float* op = A.part_o + ((size_t)inf.slot * Hq + row) * D + lane * E;
+#pragma unroll
+          for (int e = 0; e < E; ++e) op[e] = acc[h][e] * inv;
+          if (lane == 0) A.part_lse[(size_t)inf.slot * Hq + row] = lse_h;
+        }
+      }
+    }
+  }
+}
+
+// Merge s partials of one row; lane owns E consecutive dims. po points at the
+// row's first partial, consecutive partials `ostride` floats apart; lse values
+// `lstride` apart. Writes out[E] and returns the merged LSE.
+template <int E>
+__device__ __forceinline__ float merge_row(const float* po, size_t ostride, const float* pl, size_t lstride, int s,
+                                           int lane, float* out) {
+  float M = -INFINITY;
+  for (int i = lane; i < s; i += 32) M = fmaxf(M, __ldg(pl + (size_t)i * lstride));
+  M = warp_max(M);
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[e] = 0.f;
+  if (M == -INFINITY) return -INFINITY;
+  float wsum = 0.f;
+  for (int i = 0; i < s; ++i) {
+    const float w = exp2f((__ldg(pl + (size_t)i * lstride) - M) * kLog2e);
+    wsum += w;
+    const float* p = po + (size_t)i * ostride + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = fmaf(w, __ldg(p + e), out[e]);
+  }
+  const float inv = 1.f / wsum;
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[e] *= inv;
+  return M + logf(wsum);
+}
+
+// Merge after the decode kernel: one warp per (request, query head) row.
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs A) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
+  if (row >= (int64_t)A.n_req * A.Hq) return;
+  const int r = (int)(row / A.Hq), h = (int)(row % A.Hq);
+  const int beg = __ldg(A.kv_indptr + r), end = __ldg(A.kv_indptr + r + 1);
+  int slot0, s;
+  if (end > beg) {
+    if (A.mode == 0) {
+      const int k0 = beg / A.range_len, k1 = (end - 1) / A.range_len;
+      if (k0 == k1) return;  // written by the decode kernel
+      slot0 = k0 + r;
+      s = k1 - k0 + 1;
+    } else {
+      if (A.splits == 1) return;
+      slot0 = r * A.splits;
+      s = A.splits;
+    }
+  } else {
+    if (A.mode == 1 && A.splits == 1) return;  // the decode kernel wrote the empty result
+    slot0 = 0;
+    s = 0;
+  }
+  float out[E];
+  float lse = -INFINITY;
+  if (s > 0)
+    lse = merge_row<E>(A.part_o + ((size_t)slot0 * A.Hq + h) * D, (size_t)A.Hq * D, A.part_lse + (size_t)slot0 * A.Hq + h,
+                       (size_t)A.Hq, s, lane, out);
+  else
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = 0.f;
+  __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + (size_t)row * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) *reinterpret_cast<__nv_bfloat162*>(op + e) = __floats2bfloat162_rn(out[e], out[e + 1]);
+  if (A.lse && lane == 0) A.lse[row] = lse;
+}
+
+template <int E>
+__global__ void __launch_bounds__(256) merge_public_kernel(const float* __restrict__ part_o,
+                                                           const float* __restrict__ part_lse, int n_rows, int s,
+                                                           void* o, int o_dtype, float* lse) {
+  constexpr int D = 32 * E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
+  if (row >= n_rows) return;
+  float out[E];
+  const float L = merge_row<E>(part_o + (size_t)row * s * D, D, part_lse + (size_t)row * s, 1, s, lane, out);
+  if (o_dtype == STA_BF16) {
+    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(o) + (size_t)row * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) op[e] = __float2bfloat16_rn(out[e]);
+  } else {
+    float* op = static_cast<float*>(o) + (size_t)row * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) op[e] = out[e];
+  }
+  if (lse && lane == 0) lse[row] = L;
+}
+
+template <int G, int D, int HB>
+sta_status plan_t(DecodeArgs& a, int64_t T, int device) {
+  using Cfg = DecCfg<G, D, HB>;
+  auto kern = decode_kernel<G, D, HB>;
+  STA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
+  int occ = 0, sms = 0;
+  STA_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, Cfg::THREADS, Cfg::SMEM));
+  STA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+  if (occ < 1) return STA_ERR_UNSUPPORTED;
+  const int64_t ctas = (int64_t)sms * occ;
+  const int64_t per_x = ctas / (a.Hkv / HB) > 0 ? ctas / (a.Hkv / HB) : 1;  // CTAs along the token axis
+  if (a.mode == 0) {
+    int64_t rl = T > 0 ? cdiv(T, per_x) : 1;
+    if (rl < Cfg::NT) rl = Cfg::NT;
+    a.range_len = (int)rl;
+    a.n_ranges = (int)(T > 0 ? cdiv(T, rl) : 0);
+  } else {
+    const int64_t items = (int64_t)a.n_req * a.splits;
+    a.n_ranges = (int)(items < per_x ? items : per_x);
+    a.range_len = 0;
+  }
+  return STA_OK;
+}
+
+template <int G, int D, int HB>
+sta_status launch_t(const DecodeArgs& a, cudaStream_t st) {
+  using Cfg = DecCfg<G, D, HB>;
+  if (a.n_ranges > 0) {
+    decode_kernel<G, D, HB><<<dim3(a.n_ranges, a.Hkv / HB), Cfg::THREADS, Cfg::SMEM, st>>>(a);
+    STA_LAUNCH_CHECK();
+  }
+  const int64_t rows = (int64_t)a.n_req * a.Hq;
+  decode_merge_kernel<D><<<(unsigned)cdiv(rows, 8), 256, 0, st>>>(a);
+  STA_LAUNCH_CHECK();
+  return STA_OK;
+}
+
+int pick_hb(int Hkv) {
+  for (int hb = 8; hb > 1; hb >>= 1)
+    if (Hkv % hb == 0) return hb;
+  return 1;
+}
+
+template <int G, int D>
+sta_status dispatch_hb(DecodeArgs& a, int64_t T, int device, cudaStream_t st, bool plan) {
+  int hb = pick_hb(a.Hkv);
+  constexpr bool kWide = (G == 1 && D == 128);  // 32-token tiles: at most 4 heads per CTA fit
+  if (kWide && hb > 4) hb = 4;
+  switch (hb) {
+    case 8:
+      if constexpr (!kWide) return plan ? plan_t<G, D, 8>(a, T, device) : launch_t<G, D, 8>(a, st);
+      return STA_ERR_UNSUPPORTED;
+    case 4: return plan ? plan_t<G, D, 4>(a, T, device) : launch_t<G, D, 4>(a, st);
+    case 2: return plan ? plan_t<G, D, 2>(a, T, device) : launch_t<G, D, 2>(a, st);
+    default: return plan ? plan_t<G, D, 1>(a, T, device) : launch_t<G, D, 1>(a, st);
+  }
+}
+
+template <int D>
+sta_status dispatch_g(DecodeArgs& a, int64_t T, int device, cudaStream_t st, bool plan) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return dispatch_hb<1, D>(a, T, device, st, plan);
+    case 2: return dispatch_hb<2, D>(a, T, device, st, plan);
+    case 4: return dispatch_hb<4, D>(a, T, device, st, plan);
+    case 8: return dispatch_hb<8, D>(a, T, device, st, plan);
+    default: return STA_ERR_UNSUPPORTED;
+  }
+}
+
+sta_status dispatch(DecodeArgs& a, int64_t T, int device, cudaStream_t st, bool plan) {
+  if (a.d == 64) return dispatch_g<64>(a, T, device, st, plan);
+  if (a.d == 128) return dispatch_g<128>(a, T, device, st, plan);
+  return STA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+sta_status decode_plan(DecodeArgs& a, int64_t total_tokens, int device) {
+  return dispatch(a, total_tokens, device, nullptr, true);
+}
+
+size_t decode_slots(const DecodeArgs& a) {
+  if (a.mode == 0) return (size_t)a.n_ranges + (size_t)a.n_req;
+  return (size_t)a.n_req * (size_t)a.splits;
+}
+
+sta_status launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  DecodeArgs c = a;
+  return dispatch(c, 0, 0, st, false);
+}
+
+sta_status launch_merge_public(const float* part_o, const float* part_lse, int n_rows, int s, int d, void* o,
+                               int o_dtype, float* lse, cudaStream_t st) {
+  const unsigned grid = (unsigned)cdiv(n_rows, 8);
+  switch (d) {
+    case 32: merge_public_kernel<1><<<grid, 256, 0, st>>>(part_o, part_lse, n_rows, s, o, o_dtype, lse); break;
+    case 64: merge_public_kernel<2><<<grid, 256, 0, st>>>(part_o, part_lse, n_rows, s, o, o_dtype, lse); break;
+    case 128: merge_public_kernel<4><<<grid, 256, 0, st>>>(part_o, part_lse, n_rows, s, o, o_dtype, lse); break;
+    case 256: merge_public_kernel<8><<<grid, 256, 0, st>>>(part_o, part_lse, n_rows, s, o, o_dtype, lse); break;
+    default: return STA_ERR_UNSUPPORTED;
+  }
+  STA_LAUNCH_CHECK();
+  return STA_OK;
+}
+
+}  // namespace sta

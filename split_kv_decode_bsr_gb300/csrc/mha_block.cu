@@ -1,0 +1,370 @@
+// Block-wise masked MHA kernel for sm_103a (STOF, デュアルカーネル戦略 / ブロック方向カーネル:
+// Q, K, V split into sub-blocks, shared memory plus asynchronous copies overlapping
+// transfer and compute), rebuilt on Blackwell's TMA + tcgen05/TMEM:
+//
+//  * one CTA per (128-row query tile, batch x head). The tile spans outer-tile rows
+//    2t and 2t+1; its key loop runs over the union of their non-empty outer-tile
+//    columns, each half masked by its own class (empty / full / part);
+//  * warp 0 issues TMA loads (128-byte swizzle) of Q once and of K and V tiles of 64
+//    keys into a ring of stages;
+//  * warp 1 owns TMEM (256 columns: two S buffers of 64 columns and the O
+//    accumulator) and issues tcgen05.mma: S = Q K^T (M=128, N=64, K=d) and
+//    O += P V (M=128, N=d, K=64), committing completion to mbarriers;
+//  * warps 2..5 run the softmax, one query row per thread: load the S row from TMEM,
+//    apply the part-tile bitmap (byte r%8 of the 8 inner-tile words of the row),
+//    online max with lazy rescaling (O in TMEM is rescaled only when the running max
+//    grows by more than 2^8, keeping every exponential below 256), exponentials in
+//    base 2 on the MUFU unit, P rounded to bf16 into a swizzled shared-memory tile
+//    that feeds the PV MMA; at the end O / l is written as bf16 and LSE as fp32.
+// Empty outer tiles are skipped entirely ("skip, don't reset": 問題定義), full
+// tiles are never masked, iterative tiling over key blocks and one fused loop for
+// max, sum and PV follow Cleave's 複数リダクションのスケジューリング.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sta {
+namespace {
+
+constexpr int kBM = 128;       // query rows per CTA
+constexpr int kBN = 64;        // keys per tile (one outer tile)
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kMaxCols = 1024; // outer-tile columns supported (Lk <= 65536)
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+enum : int { kEmpty = -1, kFull = -2 };
+
+template <int D>
+struct BlkCfg {
+  static constexpr int KH = D / 64;                 // 128-byte column blocks of a row
+  static constexpr int STAGES = D == 64 ? 3 : 3;
+  static constexpr int Q_BYTES = kBM * D * 2;
+  static constexpr int KV_BYTES = kBN * D * 2;      // one K or V tile
+  static constexpr int P_BYTES = kBM * kBN * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_INFO = OFF_P + P_BYTES;  // then infoA[C], infoB[C], list[C]
+  static constexpr int TMEM_COLS = 256;
+  static constexpr int S_COL = 0;                   // S buffers at columns 0 and 64
+  static constexpr int O_COL = 128;
+  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(kBM, kBN, 0, 0);
+  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kBM, D, 0, 1);
+};
+
+template <int D>
+size_t blk_smem_bytes(int C) {
+  using Cfg = BlkCfg<D>;
+  return 1024 + Cfg::OFF_INFO + (size_t)C * 10 + 16;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    mha_block_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const MhaArgs A) {
+  using Cfg = BlkCfg<D>;
+  constexpr int ST = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], kv_empty[ST], s_full[2], s_free[2], p_full, o_ready;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_ntiles;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int h = (int)(bh % A.H);
+  const int hm = A.hmap.m[h];
+  const int R = A.mask.ot_rows, C = A.mask.ot_cols;
+
+  // 1024-byte aligned dynamic shared memory (128-byte swizzle atoms).
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  int32_t* infoA = reinterpret_cast<int32_t*>(smem + Cfg::OFF_INFO);
+  int32_t* infoB = infoA + C;
+  uint16_t* list = reinterpret_cast<uint16_t*>(infoB + C);
+
+  // ---- setup: barriers, TMEM, union of the two outer-tile rows' columns
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 128);
+    }
+    mbar_init(&p_full, 128);
+    mbar_init(&o_ready, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem_base, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  for (int c = threadIdx.x; c < C; c += kThreads) {
+    infoA[c] = kEmpty;
+    infoB[c] = kEmpty;
+  }
+  __syncthreads();
+  {
+    const int a0 = 2 * qt, a1 = 2 * qt + 1;
+    const int64_t rA = (int64_t)hm * R + a0, rB = (int64_t)hm * R + a1;
+    const bool hasB = a1 < R;
+    const int fA0 = A.mask.full_row_ptr[rA], fA1 = A.mask.full_row_ptr[rA + 1];
+    const int pA0 = A.mask.part_row_ptr[rA], pA1 = A.mask.part_row_ptr[rA + 1];
+    const int fB0 = hasB ? A.mask.full_row_ptr[rB] : 0, fB1 = hasB ? A.mask.full_row_ptr[rB + 1] : 0;
+    const int pB0 = hasB ? A.mask.part_row_ptr[rB] : 0, pB1 = hasB ? A.mask.part_row_ptr[rB + 1] : 0;
+    for (int t = fA0 + threadIdx.x; t < fA1; t += kThreads) infoA[A.mask.full_col_idx[t]] = kFull;
+    for (int t = pA0 + threadIdx.x; t < pA1; t += kThreads) infoA[A.mask.part_col_idx[t]] = t;
+    for (int t = fB0 + threadIdx.x; t < fB1; t += kThreads) infoB[A.mask.full_col_idx[t]] = kFull;
+    for (int t = pB0 + threadIdx.x; t < pB1; t += kThreads) infoB[A.mask.part_col_idx[t]] = t;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int n = 0;
+    for (int c0 = 0; c0 < C; c0 += 32) {
+      const int c = c0 + lane;
+      const bool ne = c < C && (infoA[c] != kEmpty || infoB[c] != kEmpty);
+      const unsigned b = __ballot_sync(0xffffffffu, ne);
+      if (ne) list[n + __popc(b & ((1u << lane) - 1u))] = (uint16_t)c;
+      n += __popc(b);
+    }
+    if (lane == 0) s_ntiles = n;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int ntiles = s_ntiles;
+  const uint32_t tmem = s_tmem_base;
+  const uint32_t sQ = smem_u32(smem + Cfg::OFF_Q);
+  const uint32_t sK = smem_u32(smem + Cfg::OFF_K);
+  const uint32_t sV = smem_u32(smem + Cfg::OFF_V);
+  const uint32_t sP = smem_u32(smem + Cfg::OFF_P);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(&q_full, Cfg::Q_BYTES);
+#pragma unroll
+      for (int kh = 0; kh < Cfg::KH; ++kh)
+        tma_load_3d(smem + Cfg::OFF_Q + kh * (kBM * 128), &tm_q, kh * 64, qt * kBM, (int)bh, &q_full);
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % ST;
+        const uint32_t round = j / ST;
+        if (!mbar_wait(&kv_empty[s], (round & 1u) ^ 1u, A.err, 0x201)) break;
+        const int key0 = list[j] * kBN;
+        mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES);
+#pragma unroll
+        for (int kh = 0; kh < Cfg::KH; ++kh)
+          tma_load_3d(smem + Cfg::OFF_K + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_k, kh * 64, key0, (int)bh,
+                      &k_full[s]);
+        mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES);
+#pragma unroll
+        for (int kh = 0; kh < Cfg::KH; ++kh)
+          tma_load_3d(smem + Cfg::OFF_V + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_v, kh * 64, key0, (int)bh,
+                      &v_full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      bool ok = mbar_wait(&q_full, 0, A.err, 0x202);
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j % ST;
+        if (!mbar_wait(&p_full, j & 1, A.err, 0x203)) return false;
+        if (!mbar_wait(&v_full[s], (j / ST) & 1, A.err, 0x204)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t ad = umma_sdesc_sw128(sP + kk * 32, 16, 1024);
+          const uint64_t bd = umma_sdesc_sw128(sV + s * Cfg::KV_BYTES + kk * 2048, kBN * 128, 1024);
+          umma_bf16(tmem + Cfg::O_COL, ad, bd, Cfg::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&kv_empty[s]);
+        umma_commit(&o_ready);
+        return true;
+      };
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int s = j % ST, sb = j & 1;
+        if (!mbar_wait(&k_full[s], (j / ST) & 1, A.err, 0x205)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, A.err, 0x206)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int kh = kk >> 2, ko = (kk & 3) * 32;
+          const uint64_t ad = umma_sdesc_sw128(sQ + kh * (kBM * 128) + ko, 16, 1024);
+          const uint64_t bd = umma_sdesc_sw128(sK + s * Cfg::KV_BYTES + kh * (kBN * 128) + ko, 16, 1024);
+          umma_bf16(tmem + Cfg::S_COL + sb * kBN, ad, bd, Cfg::IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[sb]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(ntiles - 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qd = warp & 3;             // TMEM lane quadrant of this warp
+    const int m = qd * 32 + lane;        // row within the tile
+    const int half = m >> 6, r = m & 63;
+    const int32_t* info = half ? infoB : infoA;
+    const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
+    const float c = A.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    // this row's slot in the swizzled P tile
+    uint8_t* prow = smem + Cfg::OFF_P + (m >> 3) * 1024 + (m & 7) * 128;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      const int inf = info[list[j]];
+      uint64_t bits = 0;
+      if (inf >= 0) bits = part_row_bits(A.mask.part_bitmap + (int64_t)inf * 64, r);
+      else if (inf == kFull) bits = ~0ull;
+      if (!mbar_wait(&s_full[sb], (j >> 1) & 1, A.err, 0x207)) { ok = false; break; }
+      tc_fence_after();
+      float s[64];
+      tmem_ld64_sync(t_row + Cfg::S_COL + sb * kBN, s);
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < 64; ++x) {
+        s[x] = ((bits >> x) & 1ull) ? s[x] * c : -INFINITY;
+        mx = fmaxf(mx, s[x]);
+      }
+      float alpha = 1.f;
+      bool need = false;
+      if (mx > m_ref + kRescaleThreshold) {
+        if (m_ref != -INFINITY) {
+          alpha = ex2(m_ref - mx);
+          need = true;
+        }
+        m_ref = mx;
+      }
+      l *= alpha;
+      const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pk[32];
+      float ls = 0.f;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const float p0 = ex2(s[2 * x] - mr), p1 = ex2(s[2 * x + 1] - mr);
+        ls += p0 + p1;
+        pk[x] = pack_bf16x2(p0, p1);
+      }
+      l += ls;
+      // PV(j-1) must be complete before P is overwritten or O is rescaled.
+      if (j >= 1 && !mbar_wait(&o_ready, (j - 1) & 1, A.err, 0x208)) { ok = false; break; }
+      if (__any_sync(0xffffffffu, need)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32_sync(t_row + Cfg::O_COL + c0, o);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] *= alpha;
+          tmem_st32_sync(t_row + Cfg::O_COL + c0, o);
+        }
+      }
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (m & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    // ---- epilogue: O / l (bf16) and LSE
+    const int row = qt * kBM + m;
+    if (ok && ntiles > 0) ok = mbar_wait(&o_ready, (ntiles - 1) & 1, A.err, 0x209);
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(A.o) + (bh * A.Lq + row) * (int64_t)D;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float o[32];
+      if (ntiles > 0) {
+        tmem_ld32_sync(t_row + Cfg::O_COL + c0, o);
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) o[x] = 0.f;
+      }
+      if (row < A.Lq) {
+#pragma unroll
+        for (int x = 0; x < 32; x += 8) {
+          uint4 w = make_uint4(pack_bf16x2(o[x] * inv, o[x + 1] * inv), pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv),
+                               pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv), pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv));
+          *reinterpret_cast<uint4*>(orow + c0 + x) = w;
+        }
+      }
+    }
+    if (row < A.Lq && A.lse) A.lse[bh * A.Lq + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [B*H, L, d] bf16 viewed as a 3-D tensor (d, L, B*H); box (64, rows, 1), 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, int d, int L, int BH, int rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)L, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)L * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+sta_status launch_t(const MhaArgs& a, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
+  const int BH = a.B * a.H;
+  if (!make_tmap(&tq, a.q, D, a.Lq, BH, kBM) || !make_tmap(&tk, a.k, D, a.Lk, BH, kBN) ||
+      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN))
+    return STA_ERR_CUDA;
+  const size_t smem = blk_smem_bytes<D>(a.mask.ot_cols);
+  auto kern = mha_block_kernel<D>;
+  STA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  const dim3 grid((unsigned)cdiv(a.Lq, kBM), (unsigned)BH);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  STA_LAUNCH_CHECK();
+  return STA_OK;
+}
+
+}  // namespace
+
+bool block_kernel_supports(int d, int Lk, int dtype) {
+  return dtype == STA_BF16 && (d == 64 || d == 128) && cdiv(Lk, 64) <= kMaxCols;
+}
+
+sta_status launch_mha_block(const MhaArgs& a, cudaStream_t st) {
+  if (!block_kernel_supports(a.d, a.Lk, a.dtype)) return STA_ERR_UNSUPPORTED;
+  return a.d == 64 ? launch_t<64>(a, st) : launch_t<128>(a, st);
+}
+
+}  // namespace sta

@@ -1,0 +1,141 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every declared symbol, and
+rejects bad arguments on the host before touching a GPU."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import split_kv_decode_bsr_gb300 as sta
+from split_kv_decode_bsr_gb300 import build as sta_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sta_build.build()
+    return sta.lib()
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "sta.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(sta_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_four_calls():
+    names = _declared()
+    for n in ("sta_encode_mask", "sta_mha_fwd", "sta_decode_splitkv", "sta_merge_lse"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+        assert n in sta.EXPORTED, n
+
+
+def test_status_strings(lib):
+    assert sta.status_string(0) == "ok"
+    assert "unsupported" in sta.status_string(2)
+    assert sta.status_string(99) == "unknown status"
+
+
+def _mask_struct(Hm=1, Lq=128, Lk=128):
+    s = sta._BsrMask()
+    s.n_mask_heads, s.Lq, s.Lk, s.ot_rows, s.ot_cols = Hm, Lq, Lk, (Lq + 63) // 64, (Lk + 63) // 64
+    s.full_row_ptr = s.part_row_ptr = 16  # never dereferenced on these paths
+    s.n_full = s.n_part = 0
+    return s
+
+
+def _mha(lib, **kw):
+    a = dict(q=16, k=16, v=16, o=16, lse=None, B=1, H=2, Lq=128, Lk=128, d=64, dtype=sta.STA_BF16, scale=0.125,
+             kernel=0, mask=_mask_struct(), head_map=None)
+    a.update(kw)
+    m = a["mask"]
+    return lib.sta_mha_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], C.byref(m) if m is not None else None,
+                           a["head_map"], a["B"], a["H"], a["Lq"], a["Lk"], a["d"], a["dtype"], a["scale"],
+                           a["kernel"], None)
+
+
+def test_mha_rejects_bad_arguments_on_host(lib):
+    assert _mha(lib, q=None) == sta.STA_ERR_INVALID_ARG
+    assert _mha(lib, mask=None) == sta.STA_ERR_INVALID_ARG
+    assert _mha(lib, d=96) == sta.STA_ERR_UNSUPPORTED
+    assert _mha(lib, scale=0.0) == sta.STA_ERR_INVALID_ARG
+    assert _mha(lib, scale=float("nan")) == sta.STA_ERR_INVALID_ARG
+    assert _mha(lib, Lq=100) == sta.STA_ERR_INVALID_ARG  # mask shape mismatch
+    assert _mha(lib, kernel=7) == sta.STA_ERR_INVALID_ARG
+    assert _mha(lib, dtype=5) == sta.STA_ERR_INVALID_ARG
+    assert _mha(lib, q=24) == sta.STA_ERR_UNSUPPORTED  # not 16-byte aligned
+    assert _mha(lib, mask=_mask_struct(Hm=3)) == sta.STA_ERR_INVALID_ARG  # Hm != 1, != H, no head map
+    bad_map = (C.c_int32 * 2)(0, 1)
+    assert _mha(lib, head_map=bad_map) == sta.STA_ERR_INVALID_ARG  # mask head 1 of 1
+    assert _mha(lib, dtype=sta.STA_F32, kernel=sta.STA_KERNEL_BLOCK) == sta.STA_ERR_UNSUPPORTED
+    m = _mask_struct()
+    m.n_part = 3  # part tiles without arrays
+    assert _mha(lib, mask=m) == sta.STA_ERR_INVALID_ARG
+
+
+def test_selector_is_host_only(lib):
+    m = _mask_struct()
+    m.n_full, m.n_part, m.n_valid = 1, 2, 8256
+    m.full_col_idx = m.part_col_idx = m.part_bitmap = 16
+    assert lib.sta_mha_select_kernel(C.byref(m), 1, 2, 128, 128, 64, sta.STA_F32) == sta.STA_KERNEL_ROW
+    assert lib.sta_mha_select_kernel(C.byref(m), 1, 2, 128, 128, 64, sta.STA_BF16) == sta.STA_KERNEL_BLOCK
+    m.n_valid = 30  # three computed tiles for 30 valid pairs: very sparse
+    assert lib.sta_mha_select_kernel(C.byref(m), 1, 2, 128, 128, 64, sta.STA_BF16) == sta.STA_KERNEL_ROW
+    assert lib.sta_mha_select_kernel(C.byref(m), 1, 2, 128, 128, 80, sta.STA_BF16) == -sta.STA_ERR_INVALID_ARG
+
+
+def test_encode_workspace_query_and_argument_checks(lib):
+    srcs = (sta._MaskSrc * 2)()
+    srcs[0].kind = sta.STA_MASK_PATTERN
+    srcs[1].kind = sta.STA_MASK_PATTERN
+    out = sta._BsrMask()
+    n = C.c_size_t(0)
+    assert lib.sta_encode_mask(srcs, 2, 300, 500, C.byref(out), None, C.byref(n), None) == sta.STA_OK
+    R, Cc = 5, 8
+    assert n.value >= 2 * R * Cc + 2 * R * (4 + 4 + 8)
+    assert lib.sta_encode_mask(srcs, 0, 300, 500, C.byref(out), None, C.byref(n), None) == sta.STA_ERR_INVALID_ARG
+    assert lib.sta_encode_mask(srcs, 2, 0, 500, C.byref(out), None, C.byref(n), None) == sta.STA_ERR_INVALID_ARG
+    srcs[1].kind = 9
+    assert lib.sta_encode_mask(srcs, 2, 300, 500, C.byref(out), None, C.byref(n), None) == sta.STA_ERR_INVALID_ARG
+    srcs[1].kind = sta.STA_MASK_DENSE_BITS  # dense without data
+    assert lib.sta_encode_mask(srcs, 2, 300, 500, C.byref(out), None, C.byref(n), None) == sta.STA_ERR_INVALID_ARG
+    srcs[1].kind = sta.STA_MASK_PATTERN
+    small = C.c_size_t(8)
+    assert lib.sta_encode_mask(srcs, 2, 300, 500, C.byref(out), C.c_void_p(256), C.byref(small),
+                               None) == sta.STA_ERR_WORKSPACE
+
+
+def _dec(lib, indptr, n_req, Hq=32, Hkv=8, d=128, dtype=sta.STA_BF16, splits=0, scale=0.1):
+    ind = (C.c_int32 * len(indptr))(*indptr)
+    n = C.c_size_t(0)
+    return lib.sta_decode_splitkv(None, None, None, None, ind, n_req, Hq, Hkv, d, dtype, scale, splits, None, None,
+                                  None, C.byref(n), None)
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    good = [0, 5, 9]
+    assert _dec(lib, good, 2, Hq=12, Hkv=8) == sta.STA_ERR_INVALID_ARG  # Hq % Hkv
+    assert _dec(lib, good, 2, Hq=24, Hkv=8) == sta.STA_ERR_UNSUPPORTED  # group of 3
+    assert _dec(lib, good, 2, d=96) == sta.STA_ERR_UNSUPPORTED
+    assert _dec(lib, good, 2, dtype=sta.STA_F32) == sta.STA_ERR_UNSUPPORTED
+    assert _dec(lib, [0, 5, 3], 2) == sta.STA_ERR_INVALID_ARG  # non-monotone kv_indptr
+    assert _dec(lib, [1, 5, 9], 2) == sta.STA_ERR_INVALID_ARG  # does not start at 0
+    assert _dec(lib, good, 2, splits=-1) == sta.STA_ERR_INVALID_ARG
+    assert _dec(lib, good, 2, scale=-1.0) == sta.STA_ERR_INVALID_ARG
+    assert _dec(lib, good, 0) == sta.STA_ERR_INVALID_ARG
+
+
+def test_merge_rejects_bad_arguments_on_host(lib):
+    P = C.c_void_p(256)
+    assert lib.sta_merge_lse(P, P, 4, 0, 64, P, 0, None, None) == sta.STA_ERR_INVALID_ARG
+    assert lib.sta_merge_lse(P, P, 4, 2, 48, P, 0, None, None) == sta.STA_ERR_UNSUPPORTED
+    assert lib.sta_merge_lse(P, P, 4, 2, 64, P, 7, None, None) == sta.STA_ERR_INVALID_ARG
+    assert lib.sta_merge_lse(None, P, 4, 2, 64, P, 0, None, None) == sta.STA_ERR_INVALID_ARG
+    assert lib.sta_merge_lse(None, None, 0, 2, 64, None, 0, None, None) == sta.STA_OK

@@ -1,0 +1,68 @@
+"""GPU mask encoder vs the oracle's reference encoder: bit-exact on every array and count."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from _util import gpu_sources
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(mask_heads, Lq, Lk, dev):
+    import split_kv_decode_bsr_gb300 as sta
+
+    ref = oracle.encode_mask(mask_heads, Lq, Lk)
+    got = sta.sta_encode_mask(gpu_sources(mask_heads, dev), Lq, Lk).host_arrays()
+    assert (got["n_full"], got["n_part"], got["n_valid"]) == (ref["n_full"], ref["n_part"], ref["n_valid"])
+    for key in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    np.testing.assert_array_equal(got["part_bitmap"], ref["part_bitmap"])
+    return ref
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_ok):
+    import torch
+
+    return torch.device("cuda", 0)
+
+
+@pytest.mark.parametrize("Lq,Lk", [(1, 1), (7, 9), (8, 8), (63, 64), (64, 63), (65, 130), (130, 65), (200, 200),
+                                   (300, 1000)])
+@pytest.mark.parametrize("density", [0.0, 0.05, 0.5, 1.0])
+def test_random_masks_all_kinds(dev, Lq, Lk, density):
+    u8 = [W.random_mask_u8(11, 7, Lq, Lk, density, salt=s) for s in range(3)]
+    heads = [W.MaskHead("u8", data=u8[0]), W.MaskHead("bits", data=W.pack_bits(u8[1])),
+             W.MaskHead("u8", data=u8[2]), W.pattern(causal=True, win_lo=-20, n_global_cols=3),
+             W.pattern(win_lo=-7, win_hi=70)]
+    _check(heads, Lq, Lk, dev)
+
+
+def test_more_than_one_launch_batch_of_heads(dev):
+    # 40 mask heads > 32 per launch
+    heads = [W.MaskHead("bits", data=W.pack_bits(W.random_mask_u8(3, 7, 130, 70, 0.3, salt=s))) for s in range(40)]
+    _check(heads, 130, 70, dev)
+
+
+def test_tiny_causal_and_band(dev):
+    wl = W.tiny_causal()
+    ref = _check(wl.mask_heads, 128, 128, dev)
+    assert (ref["n_full"], ref["n_part"]) == (1, 2)
+    ref = _check(W.bert_band().mask_heads, 512, 512, dev)
+    assert (ref["n_full"], ref["n_part"], ref["n_valid"]) == (8, 14, 61888)
+
+
+def test_bigbird_all_heads(dev):
+    bits = W.bigbird_mask_bits(0, 16, 4096)
+    ref = _check([W.MaskHead("bits", data=bits[h]) for h in range(16)], 4096, 4096, dev)
+    assert (ref["n_full"], ref["n_part"]) == (313 * 16, 192 * 16)
+
+
+def test_longformer_structured_and_random_head(dev):
+    L = 16384
+    wl_heads = [W.pattern(causal=True, win_lo=-255, n_global_cols=16),
+                W.MaskHead("bits", data=W.random_mask_bits(0, W.STREAM_MASK_ELEMS, L, L, 0.05))]
+    ref = _check(wl_heads, L, L, dev)
+    assert ref["n_full"] == 762 and ref["n_part"] == 759 + 65536

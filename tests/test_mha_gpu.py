@@ -1,0 +1,112 @@
+"""Masked MHA forward on the GPU (block-wise tcgen05 kernel and row-wise kernel) vs the fp64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from _util import compare, gpu_sources, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_ok):
+    import torch
+
+    return torch.device("cuda", 0)
+
+
+def _run(wl_q, wl_k, wl_v, mask_heads, head_map, scale, dtype, kernel, dev, Lq, Lk, rows=None):
+    import split_kv_decode_bsr_gb300 as sta
+
+    mask = sta.sta_encode_mask(gpu_sources(mask_heads, dev), Lq, Lk)
+    q, k, v = to_dev(wl_q, dev), to_dev(wl_k, dev), to_dev(wl_v, dev)
+    o, lse = sta.sta_mha_fwd(q, k, v, mask, head_map=head_map, scale=scale, kernel=kernel)
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    assert sta.sta_device_error() == 0
+    o_ref, lse_ref = oracle.mha_fwd(wl_q.f32, wl_k.f32, wl_v.f32, mask_heads, head_map, scale, rows=rows)
+    d = o.shape[-1]
+    if rows is not None:
+        o, lse = o.reshape(-1, d)[rows], lse.reshape(-1)[rows]
+    return compare(o, lse, o_ref, lse_ref, dtype, f"{kernel}")
+
+
+def test_tiny_causal_fp32_row_kernel(dev):
+    wl = W.tiny_causal()
+    _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "f32", "row", dev, wl.Lq, wl.Lk)
+
+
+def test_tiny_causal_fp32_auto_picks_row(dev):
+    wl = W.tiny_causal()
+    _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "f32", "auto", dev, wl.Lq, wl.Lk)
+
+
+@pytest.mark.parametrize("kernel", ["block", "row"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Lq,Lk,density", [(200, 300, 0.05), (256, 256, 0.5), (77, 1000, 0.3), (130, 65, 1.0),
+                                           (1, 1, 1.0), (64, 64, 0.01)])
+def test_random_masks_ragged(dev, kernel, d, Lq, Lk, density):
+    B, H = 2, 3
+    q = W.make_tensor(5, 1, (B, H, Lq, d), "bf16")
+    k = W.make_tensor(5, 2, (B, H, Lk, d), "bf16")
+    v = W.make_tensor(5, 3, (B, H, Lk, d), "bf16")
+    u8 = [W.random_mask_u8(7, 7, Lq, Lk, density, salt=s) for s in range(2)]
+    u8[0][::5] = 0  # fully masked rows
+    heads = [W.MaskHead("u8", data=u8[0]), W.MaskHead("bits", data=W.pack_bits(u8[1]))]
+    _run(q, k, v, heads, [1, 0, 1], 1.0 / math.sqrt(d), "bf16", kernel, dev, Lq, Lk)
+
+
+@pytest.mark.parametrize("kernel", ["block", "row"])
+def test_structured_patterns_and_single_key_rows(dev, kernel):
+    B, H, L, d = 1, 4, 320, 128
+    q = W.make_tensor(9, 1, (B, H, L, d), "bf16", 0.5)
+    k = W.make_tensor(9, 2, (B, H, L, d), "bf16", 0.5)
+    v = W.make_tensor(9, 3, (B, H, L, d), "bf16", 0.5)
+    heads = [W.pattern(causal=True), W.pattern(win_lo=-64, win_hi=64), W.pattern(causal=True, win_lo=-100,
+                                                                                  n_global_cols=16),
+             W.pattern(win_lo=0, win_hi=0)]  # diagonal only: one valid key per row
+    _run(q, k, v, heads, [0, 1, 2, 3], 0.09, "bf16", kernel, dev, L, L)
+
+
+def test_large_scores_exercise_rescaling(dev):
+    # scores spread over a wide range force many running-max updates
+    B, H, L, d = 1, 2, 512, 64
+    q = W.make_tensor(3, 1, (B, H, L, d), "bf16", 3.0)
+    k = W.make_tensor(3, 2, (B, H, L, d), "bf16", 3.0)
+    v = W.make_tensor(3, 3, (B, H, L, d), "bf16")
+    _run(q, k, v, [W.pattern(causal=True)], None, 0.125, "bf16", "block", dev, L, L)
+
+
+@pytest.mark.parametrize("kernel", ["block", "row", "auto"])
+def test_bert_band_full(dev, kernel):
+    wl = W.bert_band()
+    _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "bf16", kernel, dev, wl.Lq, wl.Lk)
+
+
+def _sample_rows(B, H, L, n, seed, extra=()):
+    rng = np.random.default_rng(seed)
+    rows = set(int(x) for x in rng.integers(0, B * H * L, n))
+    rows.update(extra)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("kernel", ["block", "row"])
+def test_bigbird_full_size_sampled_rows(dev, kernel):
+    wl = W.bigbird()
+    L = wl.Lq
+    extra = [(b * wl.H + h) * L + i for b in (0, 3) for h in (0, 15) for i in (0, 63, 64, 127, 128, 4095)]
+    rows = _sample_rows(wl.B, wl.H, L, 3000, 1, extra)
+    _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "bf16", kernel, dev, L, L, rows=rows)
+
+
+def test_longformer_full_size_sampled_rows(dev):
+    wl = W.longformer()
+    L = wl.Lq
+    extra = [h * L + i for h in (0, 17, 31) for i in (0, 1, 15, 16, 255, 256, 300, 8191, 16383)]
+    extra += [31 * L + i for i in range(0, L, 997)]
+    rows = _sample_rows(wl.B, wl.H, L, 2000, 2, extra)
+    _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "bf16", "block", dev, L, L, rows=rows)

@@ -67,42 +67,96 @@ def stream_key(seed: int, stream: int) -> int:
     return _mix_int(seed * _GAMMA + stream * 0xD1B54A32D192ED03 + 1)
 
 
+def _i64(c: int) -> np.int64:
+    """Bit pattern of a 64-bit constant as int64 (wrapping multiply is the same in both)."""
+    return np.array([c & _M64], dtype=np.uint64).view(np.int64)[0]
+
+
+_GAMMA_I, _C1_I, _C2_I = _i64(_GAMMA), _i64(_C1), _i64(_C2)
+_SH = {k: np.array([k], dtype=np.uint64) for k in (11, 27, 30, 31, 63)}
+
+
+def _mix_vec(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 finaliser on a uint64 array (multiplies done as wrapping int64).
+
+    Written with explicit ufunc calls: they are much faster than the operator
+    forms for uint64 arrays in this numpy.
+    """
+    x = np.bitwise_xor(z, np.right_shift(z, _SH[30]))
+    z = np.multiply(x.view(np.int64), _C1_I).view(np.uint64)
+    x = np.bitwise_xor(z, np.right_shift(z, _SH[27]))
+    z = np.multiply(x.view(np.int64), _C2_I).view(np.uint64)
+    return np.bitwise_xor(z, np.right_shift(z, _SH[31]))
+
+
+def _states(seed: int, stream: int, n: np.ndarray) -> np.ndarray:
+    key = _i64(stream_key(seed, stream))
+    return np.add(np.multiply(n, _GAMMA_I), key).view(np.uint64)
+
+
 def splitmix64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
     """Draws start .. start+count-1 of a stream, as uint64."""
-    key = np.uint64(stream_key(seed, stream))
-    n = np.arange(start + 1, start + count + 1, dtype=np.uint64)
-    z = key + n * np.uint64(_GAMMA)
-    z = (z ^ (z >> np.uint64(30))) * np.uint64(_C1)
-    z = (z ^ (z >> np.uint64(27))) * np.uint64(_C2)
-    return z ^ (z >> np.uint64(31))
+    return _mix_vec(_states(seed, stream, np.arange(start + 1, start + count + 1, dtype=np.int64)))
+
+
+def splitmix64_at(seed: int, stream: int, idx: np.ndarray) -> np.ndarray:
+    """Draws at arbitrary indices idx (int64 array) of a stream, as uint64."""
+    return _mix_vec(_states(seed, stream, np.add(np.asarray(idx, dtype=np.int64), 1)))
 
 
 def uniform01(x: np.ndarray) -> np.ndarray:
     """53-bit uniform in [0, 1)."""
-    return (x >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    return np.multiply(np.right_shift(x, _SH[11]).astype(np.float64), 1.0 / 9007199254740992.0)
 
 
-def normals_f32(seed: int, stream: int, count: int, chunk: int = 1 << 23) -> np.ndarray:
+_CHUNK = 1 << 17
+
+
+def _pool_map(fn, starts):
+    """Run fn(start) for every chunk start on a thread pool (numpy releases the GIL)."""
+    starts = list(starts)
+    if len(starts) <= 1:
+        for s0 in starts:
+            fn(s0)
+        return
+    import concurrent.futures as cf
+    import os
+
+    workers = min(len(starts), max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                                   else (os.cpu_count() or 1)))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(fn, starts))
+
+
+def _normals_chunk(seed: int, stream: int, s0: int, n: int) -> np.ndarray:
+    x = splitmix64(seed, stream, 2 * s0, 2 * n).reshape(n, 2)
+    u1 = np.multiply(np.add(np.right_shift(x[:, 0], _SH[11]).astype(np.float64), 1.0), 1.0 / 9007199254740992.0)
+    u2 = uniform01(x[:, 1])
+    r = np.sqrt(np.multiply(np.log(u1), -2.0))
+    return np.multiply(r, np.cos(np.multiply(u2, 2.0 * math.pi))).astype(np.float32)
+
+
+def normals_f32(seed: int, stream: int, count: int, chunk: int = _CHUNK) -> np.ndarray:
     out = np.empty(count, dtype=np.float32)
-    for s in range(0, count, chunk):
-        n = min(chunk, count - s)
-        x = splitmix64(seed, stream, 2 * s, 2 * n)
-        u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
-        u2 = uniform01(x[1::2])
-        out[s:s + n] = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)).astype(np.float32)
+
+    def work(s0):
+        n = min(chunk, count - s0)
+        out[s0:s0 + n] = _normals_chunk(seed, stream, s0, n)
+
+    _pool_map(work, range(0, count, chunk))
     return out
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns."""
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    r = ((b >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    return ((b + r) >> np.uint32(16)).astype(np.uint16)
+    r = np.add(np.bitwise_and(np.right_shift(b, np.uint32(16)), np.uint32(1)), np.uint32(0x7FFF))
+    return np.right_shift(np.add(b, r), np.uint32(16)).astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     """Exact widening of bfloat16 bit patterns to float32."""
-    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return np.left_shift(b.astype(np.uint32), np.uint32(16)).view(np.float32)
 
 
 @dataclass
@@ -117,15 +171,27 @@ class Tensor:
 
 
 def make_tensor(seed: int, stream: int, shape, dtype: str, mult: float = 1.0) -> Tensor:
-    v = normals_f32(seed, stream, int(np.prod(shape))).reshape(shape)
-    if mult != 1.0:
-        v = (v * np.float32(mult)).astype(np.float32)
-    if dtype == "bf16":
-        bits = f32_to_bf16_bits(v)
-        return Tensor(bf16_bits_to_f32(bits), bits)
-    if dtype == "f32":
-        return Tensor(v, None)
-    raise ValueError(dtype)
+    """N(0,1) * mult values of the given stream, as float32 or bf16 (plus its exact float32 widening)."""
+    count = int(np.prod(shape))
+    f32 = np.empty(count, dtype=np.float32)
+    bits = np.empty(count, dtype=np.uint16) if dtype == "bf16" else None
+    if dtype not in ("bf16", "f32"):
+        raise ValueError(dtype)
+
+    def work(s0):
+        n = min(_CHUNK, count - s0)
+        v = _normals_chunk(seed, stream, s0, n)
+        if mult != 1.0:
+            v = np.multiply(v, np.float32(mult))
+        if bits is None:
+            f32[s0:s0 + n] = v
+        else:
+            b = f32_to_bf16_bits(v)
+            bits[s0:s0 + n] = b
+            f32[s0:s0 + n] = bf16_bits_to_f32(b)
+
+    _pool_map(work, range(0, count, _CHUNK))
+    return Tensor(f32.reshape(shape), None if bits is None else bits.reshape(shape))
 
 
 @dataclass
@@ -163,20 +229,23 @@ def random_mask_u8(seed: int, stream: int, Lq: int, Lk: int, density: float, sal
     """Elementwise Bernoulli(density) mask; element (i, j) uses draw salt*Lq*Lk + i*Lk + j."""
     x = splitmix64(seed, stream, salt * Lq * Lk, Lq * Lk)
     thr = np.uint64(int(density * 9007199254740992.0))
-    return ((x >> np.uint64(11)) < thr).astype(np.uint8).reshape(Lq, Lk)
+    return np.less(np.right_shift(x, _SH[11]), thr).astype(np.uint8).reshape(Lq, Lk)
 
 
 def random_mask_bits(seed: int, stream: int, Lq: int, Lk: int, density: float,
-                     row_chunk: int = 512) -> np.ndarray:
+                     row_chunk: int = 16) -> np.ndarray:
     """As random_mask_u8 with salt 0, packed to bits row-chunk by row-chunk."""
     W = (Lk + 63) // 64
     out = np.empty((Lq, W), dtype=np.uint64)
     thr = np.uint64(int(density * 9007199254740992.0))
-    for r0 in range(0, Lq, row_chunk):
+
+    def work(r0):
         r1 = min(Lq, r0 + row_chunk)
         x = splitmix64(seed, stream, r0 * Lk, (r1 - r0) * Lk)
-        u = ((x >> np.uint64(11)) < thr).astype(np.uint8).reshape(r1 - r0, Lk)
+        u = np.less(np.right_shift(x, _SH[11]), thr).astype(np.uint8).reshape(r1 - r0, Lk)
         out[r0:r1] = pack_bits(u)
+
+    _pool_map(work, range(0, Lq, row_chunk))
     return out
 
 
@@ -274,13 +343,9 @@ def bigbird_mask_bits(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3
             for kb in rand[h][qb]:
                 rows = np.arange(r0, r1, dtype=np.uint64)
                 cols = np.arange(kb * blk, min(L, (kb + 1) * blk), dtype=np.uint64)
-                idx = ((np.uint64(h) * np.uint64(L) + rows[:, None]) * np.uint64(L) + cols[None, :])
-                key = np.uint64(stream_key(seed, STREAM_MASK_ELEMS))
-                z = key + (idx + np.uint64(1)) * np.uint64(_GAMMA)
-                z = (z ^ (z >> np.uint64(30))) * np.uint64(_C1)
-                z = (z ^ (z >> np.uint64(27))) * np.uint64(_C2)
-                z = z ^ (z >> np.uint64(31))
-                keep = ((z >> np.uint64(11)) < thr).astype(np.uint8)
+                idx = (h * L + rows[:, None].astype(np.int64)) * L + cols[None, :].astype(np.int64)
+                z = splitmix64_at(seed, STREAM_MASK_ELEMS, idx)
+                keep = np.less(np.right_shift(z, _SH[11]), thr).astype(np.uint8)
                 packed = pack_bits(keep)[:, 0]
                 bits[h, r0:r1, kb] = packed
     # clear bits past Lk in the last word
