@@ -187,6 +187,32 @@ sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const
                               float scale, int num_splits, void* o, float* lse, void* workspace,
                               size_t* workspace_bytes, sta_stream stream);
 
+/* sta_decode_splitkv_noalloc -- sta_decode_splitkv for callers that cannot
+ * allocate device memory: for example code running inside a host framework
+ * that owns every device allocation and hands out no allocator, or a serving
+ * loop that must not call cudaMalloc (which can synchronise the device) on its
+ * hot path. (The pages have no counterpart: this is a deployment variant of the
+ * split-KV decode, not part of the method.)
+ *
+ * Arguments, results and errors are those of sta_decode_splitkv without the
+ * workspace: the caller still passes q, k, v, kv_indptr, o and lse. The partial
+ * results go to one fixed 16 MiB array in the library's own device memory, which
+ * every GPU that loads the library holds until the process exits. The plan must
+ * fit it: slots * Hq * (d + 1) * 4 bytes (each part rounded up to 256) <= 16 MiB,
+ * where slots = resident CTAs + n_req when num_splits == 0 and n_req * num_splits
+ * otherwise; a larger plan returns STA_ERR_WORKSPACE and launches nothing.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. All calls
+ * share the array and it keeps the last call's contents (nothing in it needs
+ * clearing: every partial that is read is written earlier in the same call), so
+ * calls that overlap on the GPU -- on different streams, or on one device from
+ * several host threads without ordering -- race and must not be issued. Calls no
+ * cudaMalloc, cudaFree or other allocating routine. */
+sta_status sta_decode_splitkv_noalloc(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,
+                                      const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d,
+                                      sta_dtype dtype, float scale, int num_splits, void* o, float* lse,
+                                      sta_stream stream);
+
 /* sta_merge_lse -- merge s partial attention results per row:
  *   M = max_i lse_i; if M = -inf then O = 0, LSE = -inf; otherwise
  *   w_i = exp(lse_i - M), O = sum_i w_i O_i / sum_i w_i, LSE = M + log sum_i w_i.

@@ -36,8 +36,8 @@ STA_MASK_PATTERN, STA_MASK_DENSE_U8, STA_MASK_DENSE_BITS = 0, 1, 2
 STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
-EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_select_kernel", "sta_decode_splitkv", "sta_merge_lse",
-            "sta_status_string", "sta_device_error")
+EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_select_kernel", "sta_decode_splitkv",
+            "sta_decode_splitkv_noalloc", "sta_merge_lse", "sta_status_string", "sta_device_error")
 
 BIG = 1 << 40
 
@@ -77,6 +77,7 @@ def lib():
             h.sta_mha_fwd.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32, i32, P]
             h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
             h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
+            h.sta_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P]
             h.sta_merge_lse.argtypes = [P, P, i32, i32, i32, P, i32, P, P]
             h.sta_status_string.argtypes = [i32]
             h.sta_status_string.restype = C.c_char_p
@@ -288,6 +289,28 @@ def sta_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_ind
     _check("sta_decode_splitkv", h.sta_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr_dev), ind, n_req, Hq,
                                                        Hkv, d, _dtype_code(q.dtype), scale, num_splits, _ptr(o),
                                                        _ptr(lse), _ptr(workspace), C.byref(have), _stream(stream)))
+    return o, lse
+
+
+def sta_decode_splitkv_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_indptr_dev: torch.Tensor,
+                               kv_indptr_host, o: torch.Tensor, lse: Optional[torch.Tensor] = None, scale=None,
+                               num_splits: int = 0, stream=None):
+    """Split-KV decode that allocates nothing: partials go to the library's fixed 16 MiB device array.
+
+    For callers that cannot allocate device memory (see include/sta.h). The caller
+    passes the outputs o [n_req, Hq, d] (and optionally lse [n_req, Hq]); calls that
+    overlap on the GPU share that array and must not be issued.
+    """
+    n_req, Hq, d = q.shape
+    T, Hkv, dk = k.shape
+    assert dk == d and v.shape == k.shape and kv_indptr_dev.dtype == torch.int32
+    assert o.shape == q.shape and o.dtype == q.dtype
+    ind = _indptr_host(kv_indptr_host)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    _check("sta_decode_splitkv_noalloc",
+           lib().sta_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr_dev), ind, n_req, Hq, Hkv, d,
+                                            _dtype_code(q.dtype), scale, num_splits, _ptr(o), _ptr(lse),
+                                            _stream(stream)))
     return o, lse
 
 

@@ -124,7 +124,7 @@ extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, v
   return which == STA_KERNEL_BLOCK ? launch_mha_block(a, s) : launch_mha_row(a, s);
 }
 
-namespace {
+namespace sta {
 
 sta_status decode_setup(const int32_t* indptr_host, int n_req, int Hq, int Hkv, int d, sta_dtype dtype, int num_splits,
                         DecodeArgs& a, int64_t& T) {
@@ -149,8 +149,10 @@ sta_status decode_setup(const int32_t* indptr_host, int n_req, int Hq, int Hkv, 
   return decode_plan(a, T, dev);
 }
 
-inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+}  // namespace sta
 
+namespace {
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
 extern "C" sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,

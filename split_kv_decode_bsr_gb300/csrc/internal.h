@@ -46,6 +46,10 @@ struct DecodeArgs {
   int* err;
 };
 
+// Host validation of the decode arguments and the split plan (fills a, T).
+sta_status decode_setup(const int32_t* indptr_host, int n_req, int Hq, int Hkv, int d, sta_dtype dtype, int num_splits,
+                        DecodeArgs& a, int64_t& T);
+
 // Chooses the launch shape; fills range_len / n_ranges for mode 0.
 sta_status decode_plan(DecodeArgs& a, int64_t total_tokens, int device);
 size_t decode_slots(const DecodeArgs& a);
