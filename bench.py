@@ -87,11 +87,18 @@ class Dist:
             import torch
             import torch.distributed as dist
 
-            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            backend = os.environ.get("STA_BENCH_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
             if backend == "nccl":
                 torch.cuda.set_device(self.local)
             dist.init_process_group(backend)
             self.pg = dist
+
+    def _dev(self):
+        import torch
+
+        if self.pg.get_backend() == "nccl":
+            return torch.device("cuda", self.local)
+        return torch.device("cpu")
 
     def barrier(self):
         if self.pg:
@@ -102,8 +109,7 @@ class Dist:
             return x
         import torch
 
-        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        t = torch.tensor([x], dtype=torch.float64, device=self._dev())
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
@@ -112,8 +118,7 @@ class Dist:
             return x
         import torch
 
-        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        t = torch.tensor([x], dtype=torch.float64, device=self._dev())
         self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
         return float(t.item())
 
@@ -426,6 +431,8 @@ def main():
     ap.add_argument("--extra", default="bigbird,longformer,decode",
                     help="comma list of secondary workloads (bigbird, longformer, decode) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep-kernels", action="store_true",
+                    help="also time both MHA kernels on every MHA workload (selector calibration)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -456,6 +463,10 @@ def main():
     total_flops = dist.sum(mb.flops * args.steps)
     value = total_flops / dev_s / 1e12
     ms_per_step = 1e3 * dev_s / args.steps
+    kernel_ms = None
+    if args.sweep_kernels:
+        kernel_ms = {k: sum(time_device(lambda: mb.step(k), args.steps, args.warmup, dist, flush)[0]) / args.steps
+                     for k in ("block", "row")}
     e2e_s = time_e2e(mb.step_e2e, args.steps, args.warmup, dist)
     e2e_value = total_flops / e2e_s / 1e12
     kfile = "mha_block.cu" if mb.kernel == "block" else "mha_row.cu"
@@ -478,6 +489,8 @@ def main():
         "wall_s_timed_region": wall,
     }
     line["roofline"]["algorithmic_bytes_per_launch"] = mb.bytes
+    if kernel_ms:
+        line["config"]["kernel_ms"] = kernel_ms
     if dist.rank == 0 and dist.world >= 1:
         line["cpu_baseline"] = cpu_baseline(mb.wl, mb.flops, args.cpu_seconds) if dist.world == 1 else None
     del mb
@@ -518,6 +531,10 @@ def main():
                                          recorded_traffic(kf, name), peak_src),
                 "gpu_launches": steps,
             }
+            if args.sweep_kernels:
+                extras[name]["kernel_ms"] = {
+                    k: sum(time_device(lambda: b.step(k), steps, args.warmup, dist, flush)[0]) / steps
+                    for k in ("block", "row")}
             del b
         torch.cuda.empty_cache()
     line["workloads"] = extras

@@ -93,6 +93,11 @@ typedef struct {
   int32_t* part_col_idx; /* [n_part]         */
   uint64_t* part_bitmap; /* [n_part * 64]    */
   int64_t n_full, n_part, n_valid;
+  /* Optional HOST array [Hm] (caller-owned) or NULL. When set, the size query
+   * of sta_encode_mask stores each mask head's number of non-empty outer tiles
+   * there, and sta_mha_fwd then starts the query tiles of the heaviest heads
+   * first (load balance); results do not depend on it. */
+  int64_t* head_tiles;
 } sta_bsr_mask;
 
 /* sta_encode_mask -- build the two-level mask from Hm sources

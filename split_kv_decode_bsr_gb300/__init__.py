@@ -57,7 +57,8 @@ class _BsrMask(C.Structure):
     _fields_ = [("n_mask_heads", C.c_int32), ("Lq", C.c_int32), ("Lk", C.c_int32), ("ot_rows", C.c_int32),
                 ("ot_cols", C.c_int32), ("full_row_ptr", C.c_void_p), ("full_col_idx", C.c_void_p),
                 ("part_row_ptr", C.c_void_p), ("part_col_idx", C.c_void_p), ("part_bitmap", C.c_void_p),
-                ("n_full", C.c_int64), ("n_part", C.c_int64), ("n_valid", C.c_int64)]
+                ("n_full", C.c_int64), ("n_part", C.c_int64), ("n_valid", C.c_int64),
+                ("head_tiles", C.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -161,6 +162,7 @@ class BsrMask:
         self.part_row_ptr, self.part_col_idx = part_row_ptr, part_col_idx
         self.part_bitmap = part_bitmap
         self.n_full, self.n_part, self.n_valid = n_full, n_part, n_valid
+        self.head_tiles = None  # ctypes int64 array [Hm] when known
 
     def struct(self) -> _BsrMask:
         s = _BsrMask()
@@ -171,6 +173,7 @@ class BsrMask:
         s.part_col_idx = self.part_col_idx.data_ptr() if self.n_part else None
         s.part_bitmap = self.part_bitmap.data_ptr() if self.n_part else None
         s.n_full, s.n_part, s.n_valid = self.n_full, self.n_part, self.n_valid
+        s.head_tiles = C.cast(self.head_tiles, C.c_void_p) if self.head_tiles is not None else None
         return s
 
     def host_arrays(self) -> dict:
@@ -203,6 +206,8 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
     frp = torch.empty(Hm * R + 1, dtype=torch.int32, device=dev)
     prp = torch.empty(Hm * R + 1, dtype=torch.int32, device=dev)
     out.full_row_ptr, out.part_row_ptr = frp.data_ptr(), prp.data_ptr()
+    head_tiles = (C.c_int64 * Hm)()
+    out.head_tiles = C.cast(head_tiles, C.c_void_p)
     st = _stream(stream)
     _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
     nf, npart, nv = int(out.n_full), int(out.n_part), int(out.n_valid)
@@ -211,7 +216,9 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
     pbm = torch.empty(max(npart, 1) * 64, dtype=torch.int64, device=dev)
     out.full_col_idx, out.part_col_idx, out.part_bitmap = fci.data_ptr(), pci.data_ptr(), pbm.data_ptr()
     _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
-    return BsrMask(Hm, Lq, Lk, frp, fci[:nf], prp, pci[:npart], pbm[:npart * 64], nf, npart, nv)
+    m = BsrMask(Hm, Lq, Lk, frp, fci[:nf], prp, pci[:npart], pbm[:npart * 64], nf, npart, nv)
+    m.head_tiles = head_tiles
+    return m
 
 
 # ---------------------------------------------------------------------------

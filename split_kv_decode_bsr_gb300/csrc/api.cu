@@ -3,6 +3,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "internal.h"
 
 namespace sta {
@@ -32,10 +34,13 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 //          softmax of 64x64 scores;   t_b = (n_full + n_part) * 4096 * kBlockPair
 //   row:   every valid (q, k) pair costs 4*d FMA-pipe flops plus a gather;
 //          t_r = n_valid * d * kRowPair
-// with a fixed per-launch cost added to the block kernel. The constants are
-// calibrated on GB300 by the bench's selector sweep.
-constexpr double kBlockPairPerD = 1.0 / 64.0;  // relative cost of one computed pair per unit d (block)
-constexpr double kRowPairPerD = 1.0 / 2.0;     // relative cost of one valid pair per unit d (row)
+// The constants come from GB300 measurements (bench.py --sweep-kernels): the
+// block kernel spends about 0.55 ns per computed pair at d = 64 (BigBird) and
+// 0.86 ns at d = 128 (Longformer), the row kernel about 59 ns and 127 ns per
+// valid pair, so the row kernel wins only below ~1% valid density inside the
+// non-empty tiles.
+constexpr double kBlockPairPerD = 1.0 / 64.0;   // relative cost of one computed pair per unit d (block)
+constexpr double kRowPairPerD = 100.0 / 64.0;   // relative cost of one valid pair per unit d (row)
 
 int select_kernel(const sta_bsr_mask* m, int d, int Lk, sta_dtype dtype) {
   if (dtype != STA_BF16 || !block_kernel_supports(d, Lk, dtype)) return STA_KERNEL_ROW;
@@ -111,6 +116,13 @@ extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, v
     else return STA_ERR_INVALID_ARG;
     if (mh < 0 || mh >= Hm) return STA_ERR_INVALID_ARG;
     a.hmap.m[h] = (uint16_t)mh;
+  }
+  // launch order of the heads: heaviest mask heads first when their tile counts are known
+  for (int h = 0; h < H; ++h) a.hmap.order[h] = (uint16_t)h;
+  if (mask->head_tiles) {
+    const int64_t* w = mask->head_tiles;
+    std::stable_sort(a.hmap.order, a.hmap.order + H,
+                     [&](uint16_t x, uint16_t y) { return w[a.hmap.m[x]] > w[a.hmap.m[y]]; });
   }
   int which = kernel == STA_KERNEL_AUTO ? select_kernel(mask, d, Lk, dtype) : kernel;
   if (which == STA_KERNEL_BLOCK && !block_kernel_supports(d, Lk, dtype)) return STA_ERR_UNSUPPORTED;

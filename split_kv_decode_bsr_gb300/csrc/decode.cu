@@ -36,8 +36,10 @@ struct DecCfg {
   static constexpr int NT = TG > 8 ? TG : 8;    // tokens per tile
   static constexpr int GROUPS = NT / TG;
   static constexpr int TILE_BYTES = NT * HB * D * 2;  // K or V part of one stage
-  static constexpr int STAGES_RAW = 196608 / (2 * TILE_BYTES);
+  // ~96 KiB of stages so that two CTAs (16 consumer warps) share an SM
+  static constexpr int STAGES_RAW = 98304 / (2 * TILE_BYTES);
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
+  static_assert(2 * STAGES * TILE_BYTES <= 200 * 1024, "decode stages exceed shared memory");
   static constexpr int SMEM = STAGES * 2 * TILE_BYTES;
   static constexpr int THREADS = (HB + 1) * 32;
 };

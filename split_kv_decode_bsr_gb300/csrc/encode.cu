@@ -5,6 +5,8 @@
 // Three kernels per call: classify (one CTA per (mask head, OT row), warp-level
 // popcounts of the inner-tile words), a single-CTA scan of the per-row counts into
 // row_ptr, and fill (ballot-prefix positions, then the bitmaps of part tiles).
+#include <vector>
+
 #include "common.cuh"
 
 namespace sta {
@@ -307,10 +309,24 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
   if (query) {
     long long h_tot[3] = {0, 0, 0};
     STA_CUDA_TRY(cudaMemcpyAsync(h_tot, totals, sizeof(h_tot), cudaMemcpyDeviceToHost, st));
+    std::vector<int32_t> rows;
+    if (out->head_tiles) {  // per-head tile counts from the two row_ptr arrays
+      rows.resize(2 * ((size_t)Hm * R + 1));
+      STA_CUDA_TRY(cudaMemcpyAsync(rows.data(), out->full_row_ptr, sizeof(int32_t) * (Hm * R + 1),
+                                   cudaMemcpyDeviceToHost, st));
+      STA_CUDA_TRY(cudaMemcpyAsync(rows.data() + Hm * R + 1, out->part_row_ptr, sizeof(int32_t) * (Hm * R + 1),
+                                   cudaMemcpyDeviceToHost, st));
+    }
     STA_CUDA_TRY(cudaStreamSynchronize(st));
     out->n_full = h_tot[0];
     out->n_part = h_tot[1];
     out->n_valid = h_tot[2];
+    if (out->head_tiles) {
+      const int32_t* f = rows.data();
+      const int32_t* p = rows.data() + Hm * R + 1;
+      for (int h = 0; h < Hm; ++h)
+        out->head_tiles[h] = (int64_t)(f[(h + 1) * R] - f[h * R]) + (int64_t)(p[(h + 1) * R] - p[h * R]);
+    }
     return STA_OK;
   }
   for (int h0 = 0; h0 < Hm; h0 += kMaxSrcPerLaunch) {

@@ -7,7 +7,8 @@ namespace sta {
 constexpr int kMaxHeads = 1024;
 
 struct HeadMap {
-  uint16_t m[kMaxHeads];  // attention head -> mask head
+  uint16_t m[kMaxHeads];      // attention head -> mask head
+  uint16_t order[kMaxHeads];  // launch rank -> attention head (heaviest mask heads first)
 };
 
 struct MhaArgs {

@@ -8,14 +8,18 @@
 //  * warp 0 issues TMA loads (128-byte swizzle) of Q once and of K and V tiles of 64
 //    keys into a ring of stages;
 //  * warp 1 owns TMEM (256 columns: two S buffers of 64 columns and the O
-//    accumulator) and issues tcgen05.mma: S = Q K^T (M=128, N=64, K=d) and
-//    O += P V (M=128, N=d, K=64), committing completion to mbarriers;
+//    accumulator) and issues tcgen05.mma: S = Q K^T (M=128, N=64, K=d, both operands
+//    from shared memory) and O += P V (M=128, N=d, K=64, P read from TMEM),
+//    committing completion to mbarriers;
 //  * warps 2..5 run the softmax, one query row per thread: load the S row from TMEM,
-//    apply the part-tile bitmap (byte r%8 of the 8 inner-tile words of the row),
-//    online max with lazy rescaling (O in TMEM is rescaled only when the running max
-//    grows by more than 2^8, keeping every exponential below 256), exponentials in
-//    base 2 on the MUFU unit, P rounded to bf16 into a swizzled shared-memory tile
-//    that feeds the PV MMA; at the end O / l is written as bf16 and LSE as fp32.
+//    apply the part-tile bitmap (byte r%8 of the 8 inner-tile words of the row, staged
+//    in shared memory by the TMA warp), online max with lazy rescaling (O in TMEM is
+//    rescaled only when the running max grows by more than 2^8, keeping every
+//    exponential below 256), exponentials in base 2 on the MUFU unit, and P rounded
+//    to bf16 and stored back into the first 32 columns of its own S buffer, where the
+//    PV MMA reads it; at the end O / l is written as bf16 and LSE as fp32.
+//  * two CTAs share an SM (256 TMEM columns and < 114 KB of shared memory each), so
+//    one CTA's softmax overlaps the other's MMAs and loads.
 // Empty outer tiles are skipped entirely ("skip, don't reset": 問題定義), full
 // tiles are never masked, iterative tiling over key blocks and one fused loop for
 // max, sum and PV follow Cleave's 複数リダクションのスケジューリング.
@@ -39,17 +43,16 @@ enum : int { kEmpty = -1, kFull = -2 };
 template <int D>
 struct BlkCfg {
   static constexpr int KH = D / 64;                 // 128-byte column blocks of a row
-  static constexpr int STAGES = D == 64 ? 3 : 3;
+  static constexpr int STAGES = D == 64 ? 4 : 2;
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = kBN * D * 2;      // one K or V tile
-  static constexpr int P_BYTES = kBM * kBN * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_INFO = OFF_P + P_BYTES;  // then infoA[C], infoB[C], list[C]
+  static constexpr int OFF_BM = OFF_V + STAGES * KV_BYTES;  // per stage: part bitmaps of both halves (2 x 512 B)
+  static constexpr int OFF_INFO = OFF_BM + STAGES * 1024;  // then infoA[C], infoB[C], list[C]
   static constexpr int TMEM_COLS = 256;
-  static constexpr int S_COL = 0;                   // S buffers at columns 0 and 64
+  static constexpr int S_COL = 0;                   // S buffers at columns 0 and 64; P(j) over S(j)'s first 32
   static constexpr int O_COL = 128;
   static constexpr uint32_t IDESC_QK = umma_idesc_bf16(kBM, kBN, 0, 0);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kBM, D, 0, 1);
@@ -58,24 +61,27 @@ struct BlkCfg {
 template <int D>
 size_t blk_smem_bytes(int C) {
   using Cfg = BlkCfg<D>;
-  return 1024 + Cfg::OFF_INFO + (size_t)C * 10 + 16;
+  return 1024 + Cfg::OFF_INFO + (size_t)C * 10 + 16;  // OFF_INFO includes the bitmap stages
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     mha_block_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const MhaArgs A) {
   using Cfg = BlkCfg<D>;
   constexpr int ST = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], kv_empty[ST], s_full[2], s_free[2], p_full, o_ready;
+  // Per S/P buffer b (tile j uses b = j & 1): s_full[b] S(j) is in TMEM; p_full[b] P(j) is in TMEM
+  // (all 128 softmax threads); s_free[b] PV(j) has completed (committed by the MMA warp).
+  __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], kv_empty[ST], s_full[2], s_free[2], p_full[2];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_ntiles;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int h = (int)(bh % A.H);
+  // blockIdx.y enumerates (head rank, batch): the heaviest heads' tiles are dispatched first
+  const int h = A.hmap.order[blockIdx.y / A.B];
+  const int64_t bh = (int64_t)(blockIdx.y % A.B) * A.H + h;
   const int hm = A.hmap.m[h];
   const int R = A.mask.ot_rows, C = A.mask.ot_cols;
 
@@ -96,10 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
+      mbar_init(&s_free[s], 1);
+      mbar_init(&p_full[s], 128);
     }
-    mbar_init(&p_full, 128);
-    mbar_init(&o_ready, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -144,7 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + Cfg::OFF_Q);
   const uint32_t sK = smem_u32(smem + Cfg::OFF_K);
   const uint32_t sV = smem_u32(smem + Cfg::OFF_V);
-  const uint32_t sP = smem_u32(smem + Cfg::OFF_P);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -160,12 +164,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % ST;
         const uint32_t round = j / ST;
         if (!mbar_wait(&kv_empty[s], (round & 1u) ^ 1u, A.err, 0x201)) break;
-        const int key0 = list[j] * kBN;
-        mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES);
+        const int col = list[j], key0 = col * kBN;
+        const int ia = infoA[col], ib = infoB[col];
+        mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES + (ia >= 0 ? 512 : 0) + (ib >= 0 ? 512 : 0));
 #pragma unroll
         for (int kh = 0; kh < Cfg::KH; ++kh)
           tma_load_3d(smem + Cfg::OFF_K + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_k, kh * 64, key0, (int)bh,
                       &k_full[s]);
+        // the 64 inner-tile words of each half's part tile, for the softmax threads
+        if (ia >= 0) bulk_g2s(smem + Cfg::OFF_BM + s * 1024, A.mask.part_bitmap + (int64_t)ia * 64, 512, &k_full[s]);
+        if (ib >= 0)
+          bulk_g2s(smem + Cfg::OFF_BM + s * 1024 + 512, A.mask.part_bitmap + (int64_t)ib * 64, 512, &k_full[s]);
         mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES);
 #pragma unroll
         for (int kh = 0; kh < Cfg::KH; ++kh)
@@ -178,18 +187,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&q_full, 0, A.err, 0x202);
       auto issue_pv = [&](int j) -> bool {
-        const int s = j % ST;
-        if (!mbar_wait(&p_full, j & 1, A.err, 0x203)) return false;
+        const int s = j % ST, sb = j & 1;
+        if (!mbar_wait(&p_full[sb], (j >> 1) & 1, A.err, 0x203)) return false;
         if (!mbar_wait(&v_full[s], (j / ST) & 1, A.err, 0x204)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = umma_sdesc_sw128(sP + kk * 32, 16, 1024);
           const uint64_t bd = umma_sdesc_sw128(sV + s * Cfg::KV_BYTES + kk * 2048, kBN * 128, 1024);
-          umma_bf16(tmem + Cfg::O_COL, ad, bd, Cfg::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + Cfg::O_COL, tmem + Cfg::S_COL + sb * kBN + kk * 8, bd, Cfg::IDESC_PV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&kv_empty[s]);
-        umma_commit(&o_ready);
+        umma_commit(&s_free[sb]);
         return true;
       };
       for (int j = 0; ok && j < ntiles; ++j) {
@@ -219,49 +228,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = A.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    // this row's slot in the swizzled P tile
-    uint8_t* prow = smem + Cfg::OFF_P + (m >> 3) * 1024 + (m & 7) * 128;
     for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1;
-      const int inf = info[list[j]];
-      uint64_t bits = 0;
-      if (inf >= 0) bits = part_row_bits(A.mask.part_bitmap + (int64_t)inf * 64, r);
-      else if (inf == kFull) bits = ~0ull;
+      const int sb = j & 1, st = j % ST;
+      const int inf = info[list[j]];  // the same for every row of this warp (one half per warp)
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, A.err, 0x207)) { ok = false; break; }
       tc_fence_after();
       float s[64];
       tmem_ld64_sync(t_row + Cfg::S_COL + sb * kBN, s);
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int x = 0; x < 64; ++x) {
-        s[x] = ((bits >> x) & 1ull) ? s[x] * c : -INFINITY;
-        mx = fmaxf(mx, s[x]);
-      }
+      uint32_t pk[32];
       float alpha = 1.f;
       bool need = false;
-      if (mx > m_ref + kRescaleThreshold) {
-        if (m_ref != -INFINITY) {
-          alpha = ex2(m_ref - mx);
-          need = true;
-        }
-        m_ref = mx;
-      }
-      l *= alpha;
-      const float mr = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t pk[32];
-      float ls = 0.f;
+      if (inf == kEmpty) {
+        // no valid key of this tile for these rows: their P row is zero, m and l unchanged
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        const float p0 = ex2(s[2 * x] - mr), p1 = ex2(s[2 * x + 1] - mr);
-        ls += p0 + p1;
-        pk[x] = pack_bf16x2(p0, p1);
+        for (int x = 0; x < 32; ++x) pk[x] = 0u;
+      } else {
+        if (inf >= 0) {  // part tile: apply this row's 64-bit mask from the inner-tile words
+          if (!mbar_wait(&k_full[st], (j / ST) & 1, A.err, 0x20a)) { ok = false; break; }
+          const uint64_t* words = reinterpret_cast<const uint64_t*>(smem + Cfg::OFF_BM + st * 1024 + half * 512);
+          const uint64_t bits = part_row_bits(words, r);
+          const uint32_t lo = (uint32_t)bits, hi = (uint32_t)(bits >> 32);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            s[x] = ((lo >> x) & 1u) ? s[x] : -INFINITY;
+            s[x + 32] = ((hi >> x) & 1u) ? s[x + 32] : -INFINITY;
+          }
+        }
+        float m8[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) m8[x] = fmaxf(s[x], s[x + 8]);
+#pragma unroll
+        for (int x = 16; x < 64; x += 8)
+#pragma unroll
+          for (int y = 0; y < 8; ++y) m8[y] = fmaxf(m8[y], s[x + y]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * c;
+        if (mx > m_ref + kRescaleThreshold) {
+          if (m_ref != -INFINITY) {
+            alpha = ex2(m_ref - mx);
+            need = true;
+          }
+          m_ref = mx;
+        }
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        float l8[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) l8[x] = 0.f;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float p0 = ex2(fmaf(s[2 * x], c, neg_m)), p1 = ex2(fmaf(s[2 * x + 1], c, neg_m));
+          l8[x & 7] += p0 + p1;
+          pk[x] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
-      l += ls;
-      // PV(j-1) must be complete before P is overwritten or O is rescaled.
-      if (j >= 1 && !mbar_wait(&o_ready, (j - 1) & 1, A.err, 0x208)) { ok = false; break; }
       if (__any_sync(0xffffffffu, need)) {
+        // O may only be rescaled once PV(j-1) has completed (its buffer's s_free phase)
+        if (j >= 1 && !mbar_wait(&s_free[(j - 1) & 1], ((j - 1) >> 1) & 1, A.err, 0x208)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -269,21 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32_sync(t_row + Cfg::O_COL + c0, o);
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] *= alpha;
-          tmem_st32_sync(t_row + Cfg::O_COL + c0, o);
+          tmem_st32_sync(t_row + Cfg::O_COL + c0, reinterpret_cast<const uint32_t*>(o));
         }
       }
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (m & 7)) << 4)) = v;
-      }
-      fence_proxy_async_smem();
+      // P(j), bf16 pairs, over the first 32 columns of S(j) (already in registers)
+      tmem_st32_sync(t_row + Cfg::S_COL + sb * kBN, pk);
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive(&p_full[sb]);
     }
     // ---- epilogue: O / l (bf16) and LSE
     const int row = qt * kBM + m;
-    if (ok && ntiles > 0) ok = mbar_wait(&o_ready, (ntiles - 1) & 1, A.err, 0x209);
+    if (ok && ntiles > 0) ok = mbar_wait(&s_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.err, 0x209);
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(A.o) + (bh * A.Lq + row) * (int64_t)D;
