@@ -146,15 +146,28 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
       l = l * alpha + warp_sum(p);
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] *= alpha;
-      uint32_t vb = hb;
-      while (vb) {
-        const int src = __ffs(vb) - 1;
-        vb &= vb - 1;
-        const float pj = __shfl_sync(0xffffffffu, p, src);
-        float x[E];
-        IO::load_lane(A.v, kv0 + j0 + src, lane, x);
+      if (__popc(hb) >= 8 && j0 + 32 <= A.Lk) {
+        // dense chunk (all 32 keys in range): all 32 V rows, loads independent of the
+        // accumulation (p = 0 for masked keys)
+#pragma unroll 8
+        for (int src = 0; src < 32; ++src) {
+          const float pj = __shfl_sync(0xffffffffu, p, src);
+          float x[E];
+          IO::load_lane(A.v, kv0 + j0 + src, lane, x);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, x[e], acc[e]);
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, x[e], acc[e]);
+        }
+      } else {
+        uint32_t vb = hb;
+        while (vb) {
+          const int src = __ffs(vb) - 1;
+          vb &= vb - 1;
+          const float pj = __shfl_sync(0xffffffffu, p, src);
+          float x[E];
+          IO::load_lane(A.v, kv0 + j0 + src, lane, x);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, x[e], acc[e]);
+        }
       }
       m = m_new;
     }
