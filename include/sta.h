@@ -232,6 +232,11 @@ sta_status sta_merge_lse(const float* part_o, const float* part_lse, int n_rows,
 /* Static string describing a status code. */
 const char* sta_status_string(sta_status status);
 
+/* The cudaError_t behind the most recent STA_ERR_CUDA returned by any call of
+ * this library (process-wide; 0 if none), and its description. */
+int sta_last_cuda_error(void);
+const char* sta_last_cuda_error_string(void);
+
 /* Device error word of the current device: kernels whose internal waits
  * (mbarrier phases, bounded to about 2 s) give up record a nonzero code here
  * instead of hanging; 0 means no such event. Copies the word to *code

@@ -37,7 +37,8 @@ STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
 EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_select_kernel", "sta_decode_splitkv",
-            "sta_decode_splitkv_noalloc", "sta_merge_lse", "sta_status_string", "sta_device_error")
+            "sta_decode_splitkv_noalloc", "sta_merge_lse", "sta_status_string", "sta_device_error",
+            "sta_last_cuda_error", "sta_last_cuda_error_string")
 
 BIG = 1 << 40
 
@@ -45,7 +46,10 @@ BIG = 1 << 40
 class StaError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        msg = f"{fn} failed: {status_string(status)} ({status})"
+        if status == STA_ERR_CUDA:
+            msg += f": {lib().sta_last_cuda_error_string().decode()} ({lib().sta_last_cuda_error()})"
+        super().__init__(msg)
 
 
 class _MaskSrc(C.Structure):
@@ -83,8 +87,11 @@ def lib():
             h.sta_status_string.argtypes = [i32]
             h.sta_status_string.restype = C.c_char_p
             h.sta_device_error.argtypes = [C.POINTER(C.c_int), i32]
+            h.sta_last_cuda_error.argtypes = []
+            h.sta_last_cuda_error_string.argtypes = []
+            h.sta_last_cuda_error_string.restype = C.c_char_p
             for n in EXPORTED:
-                if n not in ("sta_status_string",):
+                if n not in ("sta_status_string", "sta_last_cuda_error_string"):
                     getattr(h, n).restype = C.c_int
             _lib_handle = h
     return _lib_handle

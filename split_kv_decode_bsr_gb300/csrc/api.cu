@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 
@@ -11,6 +12,9 @@ namespace sta {
 
 // Device error word written by bounded waits that time out (first code wins).
 __device__ int g_dev_error = 0;
+
+static std::atomic<int> g_last_cuda_error{0};
+void note_cuda_error(cudaError_t e) { g_last_cuda_error.store((int)e); }
 
 int* device_error_word() {
   static int* cached[64] = {nullptr};
@@ -74,6 +78,12 @@ extern "C" const char* sta_status_string(sta_status s) {
     case STA_ERR_CUDA: return "CUDA runtime error";
     default: return "unknown status";
   }
+}
+
+extern "C" int sta_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+extern "C" const char* sta_last_cuda_error_string(void) {
+  return cudaGetErrorString((cudaError_t)g_last_cuda_error.load());
 }
 
 extern "C" sta_status sta_device_error(int* code, int reset) {

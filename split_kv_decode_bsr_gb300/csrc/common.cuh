@@ -54,14 +54,25 @@ __device__ __forceinline__ uint64_t part_row_bits(const uint64_t* words, int r) 
 
 }  // namespace sta
 
+namespace sta {
+// Records the CUDA error behind the most recent STA_ERR_CUDA (see sta_last_cuda_error).
+void note_cuda_error(cudaError_t e);
+}  // namespace sta
+
 #define STA_CUDA_TRY(expr)                          \
   do {                                              \
     cudaError_t e_ = (expr);                        \
-    if (e_ != cudaSuccess) return STA_ERR_CUDA;     \
+    if (e_ != cudaSuccess) {                        \
+      sta::note_cuda_error(e_);                     \
+      return STA_ERR_CUDA;                          \
+    }                                               \
   } while (0)
 
 #define STA_LAUNCH_CHECK()                          \
   do {                                              \
     cudaError_t e_ = cudaGetLastError();            \
-    if (e_ != cudaSuccess) return STA_ERR_CUDA;     \
+    if (e_ != cudaSuccess) {                        \
+      sta::note_cuda_error(e_);                     \
+      return STA_ERR_CUDA;                          \
+    }                                               \
   } while (0)

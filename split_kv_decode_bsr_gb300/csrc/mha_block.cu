@@ -43,7 +43,7 @@ enum : int { kEmpty = -1, kFull = -2 };
 template <int D>
 struct BlkCfg {
   static constexpr int KH = D / 64;                 // 128-byte column blocks of a row
-  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int STAGES = D == 64 ? 5 : 2;
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = kBN * D * 2;      // one K or V tile
   static constexpr int OFF_Q = 0;
@@ -116,6 +116,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     infoB[c] = kEmpty;
   }
   __syncthreads();
+  // Q does not depend on the column union: start its load now, under the union's latency.
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    mbar_arrive_expect_tx(&q_full, Cfg::Q_BYTES);
+#pragma unroll
+    for (int kh = 0; kh < Cfg::KH; ++kh)
+      tma_load_3d(smem + Cfg::OFF_Q + kh * (kBM * 128), &tm_q, kh * 64, qt * kBM, (int)bh, &q_full);
+  }
   {
     const int a0 = 2 * qt, a1 = 2 * qt + 1;
     const int64_t rA = (int64_t)hm * R + a0, rB = (int64_t)hm * R + a1;
@@ -152,14 +162,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ntiles == 0) mbar_wait(&q_full, 0, A.err, 0x20b);  // drain the Q load before exiting
     if (lane == 0 && ntiles > 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&q_full, Cfg::Q_BYTES);
-#pragma unroll
-      for (int kh = 0; kh < Cfg::KH; ++kh)
-        tma_load_3d(smem + Cfg::OFF_Q + kh * (kBM * 128), &tm_q, kh * 64, qt * kBM, (int)bh, &q_full);
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % ST;
         const uint32_t round = j / ST;
@@ -364,8 +368,10 @@ sta_status launch_t(const MhaArgs& a, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   const int BH = a.B * a.H;
   if (!make_tmap(&tq, a.q, D, a.Lq, BH, kBM) || !make_tmap(&tk, a.k, D, a.Lk, BH, kBN) ||
-      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN))
+      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN)) {
+    note_cuda_error(cudaErrorInvalidValue);  // tensor-map encoding refused
     return STA_ERR_CUDA;
+  }
   const size_t smem = blk_smem_bytes<D>(a.mask.ot_cols);
   auto kern = mha_block_kernel<D>;
   STA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
