@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kBM = 128;       // query rows per CTA
 constexpr int kBN = 64;        // keys per tile (one outer tile)
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kThreads = 224;  // warp 0 K loads, warp 1 MMA, warps 2..5 softmax, warp 6 V loads
 constexpr int kMaxCols = 1024; // outer-tile columns supported (Lk <= 65536)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -73,7 +73,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   // Per S/P buffer b (tile j uses b = j & 1): s_full[b] S(j) is in TMEM; p_full[b] P(j) is in TMEM
   // (all 128 softmax threads); s_free[b] PV(j) has completed (committed by the MMA warp).
-  __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], kv_empty[ST], s_full[2], s_free[2], p_full[2];
+  // K stage s is released as soon as its QK has completed (k_empty), V stage s (with the
+  // part-tile bitmaps, which the softmax reads) once its PV has completed (v_empty).
+  __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST], s_full[2], s_free[2],
+      p_full[2];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_ntiles;
 
@@ -98,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < ST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
@@ -161,29 +165,36 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t sV = smem_u32(smem + Cfg::OFF_V);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ K loads
     if (lane == 0 && ntiles == 0) mbar_wait(&q_full, 0, A.err, 0x20b);  // drain the Q load before exiting
     if (lane == 0 && ntiles > 0) {
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % ST;
-        const uint32_t round = j / ST;
-        if (!mbar_wait(&kv_empty[s], (round & 1u) ^ 1u, A.err, 0x201)) break;
-        const int col = list[j], key0 = col * kBN;
+        if (!mbar_wait(&k_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x201)) break;
+        mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES);
+#pragma unroll
+        for (int kh = 0; kh < Cfg::KH; ++kh)
+          tma_load_3d(smem + Cfg::OFF_K + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_k, kh * 64, list[j] * kBN,
+                      (int)bh, &k_full[s]);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ V loads (+ part-tile bitmaps)
+    if (lane == 0 && ntiles > 0) {
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % ST;
+        if (!mbar_wait(&v_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x20c)) break;
+        const int col = list[j];
         const int ia = infoA[col], ib = infoB[col];
-        mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES + (ia >= 0 ? 512 : 0) + (ib >= 0 ? 512 : 0));
+        mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES + (ia >= 0 ? 512 : 0) + (ib >= 0 ? 512 : 0));
 #pragma unroll
         for (int kh = 0; kh < Cfg::KH; ++kh)
-          tma_load_3d(smem + Cfg::OFF_K + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_k, kh * 64, key0, (int)bh,
-                      &k_full[s]);
-        // the 64 inner-tile words of each half's part tile, for the softmax threads
-        if (ia >= 0) bulk_g2s(smem + Cfg::OFF_BM + s * 1024, A.mask.part_bitmap + (int64_t)ia * 64, 512, &k_full[s]);
-        if (ib >= 0)
-          bulk_g2s(smem + Cfg::OFF_BM + s * 1024 + 512, A.mask.part_bitmap + (int64_t)ib * 64, 512, &k_full[s]);
-        mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES);
-#pragma unroll
-        for (int kh = 0; kh < Cfg::KH; ++kh)
-          tma_load_3d(smem + Cfg::OFF_V + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_v, kh * 64, key0, (int)bh,
+          tma_load_3d(smem + Cfg::OFF_V + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_v, kh * 64, col * kBN, (int)bh,
                       &v_full[s]);
+        // the 64 inner-tile words of each half's part tile, for the softmax threads
+        if (ia >= 0) bulk_g2s(smem + Cfg::OFF_BM + s * 1024, A.mask.part_bitmap + (int64_t)ia * 64, 512, &v_full[s]);
+        if (ib >= 0)
+          bulk_g2s(smem + Cfg::OFF_BM + s * 1024 + 512, A.mask.part_bitmap + (int64_t)ib * 64, 512, &v_full[s]);
       }
     }
   } else if (warp == 1) {
@@ -201,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           umma_bf16_ts(tmem + Cfg::O_COL, tmem + Cfg::S_COL + sb * kBN + kk * 8, bd, Cfg::IDESC_PV,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&kv_empty[s]);
+        umma_commit(&v_empty[s]);
         umma_commit(&s_free[sb]);
         return true;
       };
@@ -218,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           umma_bf16(tmem + Cfg::S_COL + sb * kBN, ad, bd, Cfg::IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[sb]);
+        umma_commit(&k_empty[s]);
         if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
       }
       if (ok) issue_pv(ntiles - 1);
@@ -248,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int x = 0; x < 32; ++x) pk[x] = 0u;
       } else {
         if (inf >= 0) {  // part tile: apply this row's 64-bit mask from the inner-tile words
-          if (!mbar_wait(&k_full[st], (j / ST) & 1, A.err, 0x20a)) { ok = false; break; }
+          if (!mbar_wait(&v_full[st], (j / ST) & 1, A.err, 0x20a)) { ok = false; break; }
           const uint64_t* words = reinterpret_cast<const uint64_t*>(smem + Cfg::OFF_BM + st * 1024 + half * 512);
           const uint64_t bits = part_row_bits(words, r);
           const uint32_t lo = (uint32_t)bits, hi = (uint32_t)(bits >> 32);
