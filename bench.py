@@ -7,7 +7,9 @@ workload (B=8, H=12, L=512, d=64, bf16). The same line carries the split-KV GQA
 decode (KV-read GB/s) and the BigBird and Longformer workloads as secondary
 objects, each with its roofline fraction against the measured GB300 peaks.
 
-A step is one sta_mha_fwd call (mask encoded once, outside the timed region).
+A step is one sta_mha_fwd_splitkv call with the library's split plan (the
+block kernel, plus the log-sum-exp merge when a head is split; mask encoded
+once, outside the timed region).
 L2 is flushed (a 256 MiB write, outside the CUDA events) before every timed
 launch. The device time is the sum of per-launch CUDA-event durations on the
 launching stream; `e2e` repeats the step through the public API with the
@@ -236,7 +238,7 @@ def valid_pairs(wl, mask_counts):
 
 
 class MhaBench:
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, num_splits=0):
         import torch
 
         import split_kv_decode_bsr_gb300 as sta
@@ -257,13 +259,24 @@ class MhaBench:
                                                 torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((wl.B, wl.H, wl.Lq), dtype=torch.float32, device=dev)
+        # split-KV plan of the block kernel (0: the library's choice from the mask's tile counts)
+        self.num_splits = num_splits
+        ws = sta.mha_splitkv_workspace_bytes(self.mask, wl.B, wl.H, wl.d, self.q.dtype, head_map=wl.head_map,
+                                             num_splits=num_splits)
+        self.split = self.kernel == "block" and ws > 256
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.hq, self.hk, self.hv = (x.cpu().pin_memory() for x in (self.q, self.k, self.v))
         self.ho = torch.empty_like(self.o, device="cpu").pin_memory()
         self.hlse = torch.empty_like(self.lse, device="cpu").pin_memory()
 
     def step(self, kernel=None):
-        self.sta.sta_mha_fwd(self.q, self.k, self.v, self.mask, head_map=self.wl.head_map, scale=self.wl.scale,
-                             kernel=kernel or "auto", o=self.o, lse=self.lse)
+        if kernel is not None:  # selector calibration: one kernel, no split
+            self.sta.sta_mha_fwd(self.q, self.k, self.v, self.mask, head_map=self.wl.head_map, scale=self.wl.scale,
+                                 kernel=kernel, o=self.o, lse=self.lse)
+            return
+        self.sta.sta_mha_fwd_splitkv(self.q, self.k, self.v, self.mask, head_map=self.wl.head_map,
+                                     scale=self.wl.scale, num_splits=self.num_splits, o=self.o, lse=self.lse,
+                                     workspace=self.ws)
 
     def step_e2e(self):
         self.q.copy_(self.hq, non_blocking=True)
@@ -282,7 +295,7 @@ class MhaBench:
         return sum(x.numel() * x.element_size() for x in (self.ho, self.hlse))
 
     def launches_per_step(self):
-        return 1
+        return 2 if self.split else 1  # block kernel (+ the merge of split heads)
 
 
 class DecodeBench:
@@ -431,6 +444,8 @@ def main():
     ap.add_argument("--extra", default="bigbird,longformer,decode",
                     help="comma list of secondary workloads (bigbird, longformer, decode) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mha-splits", type=int, default=0,
+                    help="split-KV chunks per head for the block kernel (0: the library's plan)")
     ap.add_argument("--sweep-kernels", action="store_true",
                     help="also time both MHA kernels on every MHA workload (selector calibration)")
     args = ap.parse_args()
@@ -456,7 +471,7 @@ def main():
         flush_buf.fill_(1)
 
     # ---- headline: masked MHA on the BERT-base band workload
-    mb = MhaBench(args.workload, dev)
+    mb = MhaBench(args.workload, dev, args.mha_splits)
     with ClockSampler(dist.local) as clk:
         ms, wall = time_device(mb.step, args.steps, args.warmup, dist, flush)
     dev_s = dist.max(sum(ms) / 1e3)
@@ -478,6 +493,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": mb.wl.name, "B": mb.wl.B, "H": mb.wl.H, "L": mb.wl.Lq, "d": mb.wl.d,
                    "mask": "sliding window |i-j|<=64", "valid_pairs": mb.pairs, "kernel": mb.kernel,
+                   "split_kv": "planned" if mb.split else "none",
                    "l2": "flushed before every timed launch (256 MiB write)", "parallelism": f"replicas x{dist.world}"},
         "tensor_frac": (mb.flops / avg_launch_s / 1e12) / peaks["bf16_tflops"],
         "roofline": roofline_obj("hbm", achieved, peaks["hbm_gbs"], "GB/s", recorded_traffic(kfile, mb.name),
@@ -518,18 +534,19 @@ def main():
             }
             del db
         else:
-            b = MhaBench(name, dev)
+            b = MhaBench(name, dev, args.mha_splits)
             ms, _ = time_device(b.step, steps, args.warmup, dist, flush)
             t = sum(ms) / len(ms) / 1e3
             tf = b.flops / t / 1e12
             kf = "mha_block.cu" if b.kernel == "block" else "mha_row.cu"
             extras[name] = {
                 "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": tf, "unit": "TFLOP/s", "ms_per_step": 1e3 * t,
-                "config": {"workload": b.wl.name, "valid_pairs": b.pairs, "kernel": b.kernel},
+                "config": {"workload": b.wl.name, "valid_pairs": b.pairs, "kernel": b.kernel,
+                           "split_kv": "planned" if b.split else "none", "workspace_bytes": b.ws.numel()},
                 "tensor_frac": tf / peaks["bf16_tflops"],
                 "roofline": roofline_obj("hbm", b.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
                                          recorded_traffic(kf, name), peak_src),
-                "gpu_launches": steps,
+                "gpu_launches": b.launches_per_step() * steps,
             }
             if args.sweep_kernels:
                 extras[name]["kernel_ms"] = {

@@ -157,6 +157,37 @@ sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, flo
                        const int32_t* head_map, int B, int H, int Lq, int Lk, int d, sta_dtype dtype, float scale,
                        int kernel, sta_stream stream);
 
+/* sta_mha_fwd_splitkv -- sta_mha_fwd with the key-tile loop of the block-wise
+ * kernel split (Cleave, Split演算子によるSplit-Kの対応, applied to masked
+ * prefill): the list of non-empty key tiles of each (128-row query tile, b, h)
+ * is cut into s chunks, each attended by its own CTA into a normalised fp32
+ * partial and its LSE, and the chunks are merged by log-sum-exp as in
+ * sta_merge_lse. Long rows (a dense or random head among banded ones, small
+ * B*H) then spread over many CTAs instead of one.
+ *
+ *   q .. kernel  as for sta_mha_fwd; the split applies to the block-wise
+ *                kernel only (a row-wise choice runs unsplit)
+ *   num_splits   0: the library picks s per head from mask->head_tiles (no
+ *                split when it is NULL): heads whose key tiles per query tile
+ *                exceed twice the average load of a resident CTA slot (two
+ *                per SM; each item counted with a prologue of about 4 tiles)
+ *                are cut
+ *                into chunks of about that load (at least 16 tiles, at most
+ *                32 chunks); other heads run whole;
+ *                1..1024: every head is cut into that many chunks (chunks past
+ *                a row's tile count are empty and contribute nothing)
+ *   workspace    device scratch for the partials, 256-byte aligned;
+ *                workspace == NULL sets *workspace_bytes (never 0) and
+ *                returns without touching the data pointers
+ * Results equal sta_mha_fwd's up to rounding (the merge re-normalises fp32
+ * partials). Returns STA_ERR_UNSUPPORTED when B * (sum of the heads' s)
+ * exceeds 65535, STA_ERR_WORKSPACE when *workspace_bytes is too small, and
+ * otherwise the errors of sta_mha_fwd. Asynchronous on `stream`. */
+sta_status sta_mha_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq, int Lk, int d,
+                               sta_dtype dtype, float scale, int kernel, int num_splits, void* workspace,
+                               size_t* workspace_bytes, sta_stream stream);
+
 /* Which kernel sta_mha_fwd would run for these arguments under
  * STA_KERNEL_AUTO (STA_KERNEL_BLOCK or STA_KERNEL_ROW), or a negative
  * sta_status on invalid arguments. Host only. */

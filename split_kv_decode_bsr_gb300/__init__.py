@@ -36,7 +36,7 @@ STA_MASK_PATTERN, STA_MASK_DENSE_U8, STA_MASK_DENSE_BITS = 0, 1, 2
 STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
-EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_select_kernel", "sta_decode_splitkv",
+EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_select_kernel", "sta_decode_splitkv",
             "sta_decode_splitkv_noalloc", "sta_merge_lse", "sta_status_string", "sta_device_error",
             "sta_last_cuda_error", "sta_last_cuda_error_string")
 
@@ -80,6 +80,8 @@ def lib():
             P, i32, f32, sz = C.c_void_p, C.c_int, C.c_float, C.POINTER(C.c_size_t)
             h.sta_encode_mask.argtypes = [P, i32, i32, i32, C.POINTER(_BsrMask), P, sz, P]
             h.sta_mha_fwd.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32, i32, P]
+            h.sta_mha_fwd_splitkv.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32,
+                                              i32, i32, P, sz, P]
             h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
             h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
             h.sta_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P]
@@ -260,6 +262,57 @@ def sta_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BsrMask
     st = lib().sta_mha_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), C.byref(s), hm, B, H, Lq, Lk, d,
                            _dtype_code(q.dtype), scale, _KERNELS[kernel], _stream(stream))
     _check("sta_mha_fwd", st)
+    return o, lse
+
+
+def _mha_common(q, k, v, o, lse, head_map):
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous()
+    assert k.shape == (B, H, Lk, d) and v.shape == k.shape and q.dtype == k.dtype == v.dtype
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    hm = None if head_map is None else (C.c_int32 * H)(*[int(x) for x in head_map])
+    return B, H, Lq, Lk, d, o, lse, hm
+
+
+def mha_splitkv_workspace_bytes(mask: BsrMask, B: int, H: int, d: int, dtype=torch.bfloat16, head_map=None,
+                                kernel: str = "auto", num_splits: int = 0) -> int:
+    """Workspace size sta_mha_fwd_splitkv needs for these arguments (never 0)."""
+    hm = None if head_map is None else (C.c_int32 * H)(*[int(x) for x in head_map])
+    s = mask.struct()
+    n = C.c_size_t(0)
+    _check("sta_mha_fwd_splitkv", lib().sta_mha_fwd_splitkv(None, None, None, None, None, C.byref(s), hm, B, H,
+                                                            mask.Lq, mask.Lk, d, _dtype_code(dtype),
+                                                            1.0 / math.sqrt(d), _KERNELS[kernel], num_splits, None,
+                                                            C.byref(n), None))
+    return int(n.value)
+
+
+def sta_mha_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BsrMask, head_map=None, scale=None,
+                        kernel: str = "auto", num_splits: int = 0, o: Optional[torch.Tensor] = None,
+                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """sta_mha_fwd with the block kernel's key-tile loop split into chunks merged by log-sum-exp.
+
+    num_splits 0 lets the library choose per head (from mask.head_tiles); s > 0 cuts
+    every head's key-tile list into s chunks. workspace: a uint8 device tensor of at
+    least mha_splitkv_workspace_bytes(...) bytes (allocated here when None).
+    """
+    B, H, Lq, Lk, d, o, lse, hm = _mha_common(q, k, v, o, lse, head_map)
+    s = mask.struct()
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    h = lib()
+    need = C.c_size_t(0)
+    args = (C.byref(s), hm, B, H, Lq, Lk, d, _dtype_code(q.dtype), scale, _KERNELS[kernel], num_splits)
+    _check("sta_mha_fwd_splitkv", h.sta_mha_fwd_splitkv(None, None, None, None, None, *args, None, C.byref(need),
+                                                        None))
+    if workspace is None or workspace.numel() < need.value:
+        workspace = torch.empty(int(need.value), dtype=torch.uint8, device=q.device)
+    have = C.c_size_t(workspace.numel())
+    _check("sta_mha_fwd_splitkv", h.sta_mha_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), *args,
+                                                        _ptr(workspace), C.byref(have), _stream(stream)))
     return o, lse
 
 

@@ -46,6 +46,8 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr double kBlockPairPerD = 1.0 / 64.0;   // relative cost of one computed pair per unit d (block)
 constexpr double kRowPairPerD = 100.0 / 64.0;   // relative cost of one valid pair per unit d (row)
 
+constexpr int kMaxSplitsPrefill = 1024;
+
 int select_kernel(const sta_bsr_mask* m, int d, int Lk, sta_dtype dtype) {
   if (dtype != STA_BF16 || !block_kernel_supports(d, Lk, dtype)) return STA_KERNEL_ROW;
   const double computed = (double)(m->n_full + m->n_part) * 4096.0;
@@ -102,20 +104,19 @@ extern "C" int sta_mha_select_kernel(const sta_bsr_mask* mask, int B, int H, int
   return select_kernel(mask, d, Lk, dtype);
 }
 
-extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                                  const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq, int Lk,
-                                  int d, sta_dtype dtype, float scale, int kernel, sta_stream stream) {
-  if (!q || !k || !v || !o) return STA_ERR_INVALID_ARG;
+namespace {
+
+// Shared validation of sta_mha_fwd / sta_mha_fwd_splitkv (everything but the
+// data pointers): fills the kernel arguments and the kernel to run.
+sta_status mha_prepare(const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq, int Lk, int d,
+                       sta_dtype dtype, float scale, int kernel, MhaArgs& a, int& which) {
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || H > kMaxHeads || (int64_t)B * H > 65535) return STA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return STA_ERR_INVALID_ARG;
   if (dtype != STA_BF16 && dtype != STA_F32) return STA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return STA_ERR_UNSUPPORTED;
   if (kernel < STA_KERNEL_AUTO || kernel > STA_KERNEL_ROW) return STA_ERR_INVALID_ARG;
-  sta_status st = check_mask(mask, Lq, Lk);
+  const sta_status st = check_mask(mask, Lq, Lk);
   if (st != STA_OK) return st;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return STA_ERR_UNSUPPORTED;
-  if (lse && ((uintptr_t)lse & 3u)) return STA_ERR_UNSUPPORTED;
-  MhaArgs a;
   memset(&a, 0, sizeof(a));
   const int Hm = mask->n_mask_heads;
   for (int h = 0; h < H; ++h) {
@@ -134,16 +135,73 @@ extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, v
     std::stable_sort(a.hmap.order, a.hmap.order + H,
                      [&](uint16_t x, uint16_t y) { return w[a.hmap.m[x]] > w[a.hmap.m[y]]; });
   }
-  int which = kernel == STA_KERNEL_AUTO ? select_kernel(mask, d, Lk, dtype) : kernel;
+  which = kernel == STA_KERNEL_AUTO ? select_kernel(mask, d, Lk, dtype) : kernel;
   if (which == STA_KERNEL_BLOCK && !block_kernel_supports(d, Lk, dtype)) return STA_ERR_UNSUPPORTED;
-  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
   a.mask = MaskView{mask->full_row_ptr, mask->full_col_idx, mask->part_row_ptr, mask->part_col_idx,
                     mask->part_bitmap, mask->ot_rows, mask->ot_cols};
   a.B = B; a.H = H; a.Lq = Lq; a.Lk = Lk; a.d = d; a.dtype = dtype;
   a.scale_log2 = scale * kLog2e;
+  return STA_OK;
+}
+
+sta_status mha_set_data(MhaArgs& a, const void* q, const void* k, const void* v, void* o, float* lse) {
+  if (!q || !k || !v || !o) return STA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return STA_ERR_UNSUPPORTED;
+  if (lse && ((uintptr_t)lse & 3u)) return STA_ERR_UNSUPPORTED;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
   a.err = device_error_word();
+  return STA_OK;
+}
+
+}  // namespace
+
+extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq, int Lk,
+                                  int d, sta_dtype dtype, float scale, int kernel, sta_stream stream) {
+  if (!q || !k || !v || !o) return STA_ERR_INVALID_ARG;
+  MhaArgs a;
+  int which = 0;
+  sta_status st = mha_prepare(mask, head_map, B, H, Lq, Lk, d, dtype, scale, kernel, a, which);
+  if (st != STA_OK) return st;
+  if ((st = mha_set_data(a, q, k, v, o, lse)) != STA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  return which == STA_KERNEL_BLOCK ? launch_mha_block(a, s) : launch_mha_row(a, s);
+  if (which != STA_KERNEL_BLOCK) return launch_mha_row(a, s);
+  MhaSplit plan;  // no split: one chunk per item
+  if ((st = plan_mha_split(a, nullptr, 1, -1, plan)) != STA_OK) return st;
+  return launch_mha_block(a, plan, s);
+}
+
+extern "C" sta_status sta_mha_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                                          const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq,
+                                          int Lk, int d, sta_dtype dtype, float scale, int kernel, int num_splits,
+                                          void* workspace, size_t* workspace_bytes, sta_stream stream) {
+  if (!workspace_bytes || num_splits < 0 || num_splits > kMaxSplitsPrefill) return STA_ERR_INVALID_ARG;
+  MhaArgs a;
+  int which = 0;
+  sta_status st = mha_prepare(mask, head_map, B, H, Lq, Lk, d, dtype, scale, kernel, a, which);
+  if (st != STA_OK) return st;
+  MhaSplit plan;
+  size_t need = 256;  // never zero, so that a null workspace always means "query"
+  if (which == STA_KERNEL_BLOCK) {
+    if ((st = plan_mha_split(a, mask->head_tiles, num_splits, -1, plan)) != STA_OK) return st;
+    need = std::max(need, mha_split_workspace_bytes(a, plan));
+  }
+  if (!workspace) {
+    *workspace_bytes = need;
+    return STA_OK;
+  }
+  if (*workspace_bytes < need) return STA_ERR_WORKSPACE;
+  if ((uintptr_t)workspace & 255u) return STA_ERR_UNSUPPORTED;
+  if ((st = mha_set_data(a, q, k, v, o, lse)) != STA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (which != STA_KERNEL_BLOCK) return launch_mha_row(a, s);
+  if (plan.n_split_ranks > 0) {
+    const size_t rows = (size_t)plan.ybase[plan.n_split_ranks] * (size_t)Lq;
+    plan.part_o = static_cast<float*>(workspace);
+    plan.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             (((rows * (size_t)d * sizeof(float)) + 255) & ~(size_t)255));
+  }
+  return launch_mha_block(a, plan, s);
 }
 
 namespace sta {

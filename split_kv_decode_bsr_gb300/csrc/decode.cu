@@ -290,32 +290,6 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
   }
 }
 
-// Merge s partials of one row; lane owns E consecutive dims. po points at the
-// row's first partial, consecutive partials `ostride` floats apart; lse values
-// `lstride` apart. Writes out[E] and returns the merged LSE.
-template <int E>
-__device__ __forceinline__ float merge_row(const float* po, size_t ostride, const float* pl, size_t lstride, int s,
-                                           int lane, float* out) {
-  float M = -INFINITY;
-  for (int i = lane; i < s; i += 32) M = fmaxf(M, __ldg(pl + (size_t)i * lstride));
-  M = warp_max(M);
-#pragma unroll
-  for (int e = 0; e < E; ++e) out[e] = 0.f;
-  if (M == -INFINITY) return -INFINITY;
-  float wsum = 0.f;
-  for (int i = 0; i < s; ++i) {
-    const float w = exp2f((__ldg(pl + (size_t)i * lstride) - M) * kLog2e);
-    wsum += w;
-    const float* p = po + (size_t)i * ostride + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = fmaf(w, __ldg(p + e), out[e]);
-  }
-  const float inv = 1.f / wsum;
-#pragma unroll
-  for (int e = 0; e < E; ++e) out[e] *= inv;
-  return M + logf(wsum);
-}
-
 // Merge after the decode kernel: one warp per (request, query head) row.
 template <int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs A) {

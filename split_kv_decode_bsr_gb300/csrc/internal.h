@@ -25,8 +25,32 @@ struct MhaArgs {
   int* err;          // device error word
 };
 
+// Split-KV plan of the block kernel (Cleave, Split演算子によるSplit-Kの対応 applied to
+// the key-tile loop). grid.y enumerates (launch rank, batch, chunk): rank r covers
+// grid.y indices ybase[r] .. ybase[r+1]-1 as b * s[r] + c. The key-tile list of a
+// (query tile, b, h) item with n tiles is cut into s[r] chunks, chunk c taking
+// tiles [c*n/s, (c+1)*n/s). Ranks with s > 1 form a prefix of the launch order
+// (ranks 0 .. n_split_ranks-1); their chunks write normalised fp32 partials at
+// partial row y * Lq + i (y = grid.y index), merged afterwards by log-sum-exp.
+struct MhaSplit {
+  float* part_o;     // [ybase[n_split_ranks], Lq, d] fp32, or null when nothing is split
+  float* part_lse;   // [ybase[n_split_ranks], Lq] fp32 (natural log)
+  int n_split_ranks;
+  int uniform_s;     // > 0: every rank has s = uniform_s (ybase[r] = r * B * uniform_s)
+  int n_y;           // grid.y
+  int32_t ybase[kMaxHeads + 1];
+  uint16_t s[kMaxHeads];
+};
+
+// Fills the plan: s per launch rank from num_splits (> 0: that many chunks for
+// every head) or, when num_splits == 0, from the mask heads' tile counts
+// (mask_head_tiles, may be null: no split) against the resident CTA slots of
+// `device` (-1: the current device; queried only in that last case).
+sta_status plan_mha_split(const MhaArgs& a, const int64_t* mask_head_tiles, int num_splits, int device, MhaSplit& p);
+size_t mha_split_workspace_bytes(const MhaArgs& a, const MhaSplit& p);
+
 sta_status launch_mha_row(const MhaArgs& a, cudaStream_t st);
-sta_status launch_mha_block(const MhaArgs& a, cudaStream_t st);
+sta_status launch_mha_block(const MhaArgs& a, const MhaSplit& p, cudaStream_t st);
 bool block_kernel_supports(int d, int Lk, int dtype);
 
 struct DecodeArgs {

@@ -67,7 +67,7 @@ size_t blk_smem_bytes(int C) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     mha_block_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const MhaArgs A) {
+                     const __grid_constant__ CUtensorMap tm_v, const MhaArgs A, const MhaSplit P) {
   using Cfg = BlkCfg<D>;
   constexpr int ST = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -78,13 +78,31 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST], s_full[2], s_free[2],
       p_full[2];
   __shared__ uint32_t s_tmem_base;
-  __shared__ int s_ntiles;
+  __shared__ int s_ntiles, s_jb;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x;
-  // blockIdx.y enumerates (head rank, batch): the heaviest heads' tiles are dispatched first
-  const int h = A.hmap.order[blockIdx.y / A.B];
-  const int64_t bh = (int64_t)(blockIdx.y % A.B) * A.H + h;
+  // blockIdx.y enumerates (head rank, batch, chunk): the heaviest heads' tiles are dispatched first
+  const int y = blockIdx.y;
+  int rank, n_split, off;
+  if (P.uniform_s > 0) {
+    n_split = P.uniform_s;
+    rank = y / (A.B * n_split);
+    off = y - rank * A.B * n_split;
+  } else {
+    int lo = 0, hi = A.H;  // P.ybase[lo] <= y < P.ybase[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (P.ybase[mid] <= y) lo = mid;
+      else hi = mid;
+    }
+    rank = lo;
+    n_split = P.s[lo];
+    off = y - P.ybase[lo];
+  }
+  const int bi = off / n_split, chunk = off - bi * n_split;
+  const int h = A.hmap.order[rank];
+  const int64_t bh = (int64_t)bi * A.H + h;
   const int hm = A.hmap.m[h];
   const int R = A.mask.ot_rows, C = A.mask.ot_cols;
 
@@ -153,12 +171,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (ne) list[n + __popc(b & ((1u << lane) - 1u))] = (uint16_t)c;
       n += __popc(b);
     }
-    if (lane == 0) s_ntiles = n;
+    if (lane == 0) {  // this CTA's chunk of the column list
+      const int jb = (int)((int64_t)chunk * n / n_split);
+      s_jb = jb;
+      s_ntiles = (int)((int64_t)(chunk + 1) * n / n_split) - jb;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const int ntiles = s_ntiles;
+  const uint16_t* lst = list + s_jb;
   const uint32_t tmem = s_tmem_base;
   const uint32_t sQ = smem_u32(smem + Cfg::OFF_Q);
   const uint32_t sK = smem_u32(smem + Cfg::OFF_K);
@@ -174,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES);
 #pragma unroll
         for (int kh = 0; kh < Cfg::KH; ++kh)
-          tma_load_3d(smem + Cfg::OFF_K + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_k, kh * 64, list[j] * kBN,
+          tma_load_3d(smem + Cfg::OFF_K + s * Cfg::KV_BYTES + kh * (kBN * 128), &tm_k, kh * 64, lst[j] * kBN,
                       (int)bh, &k_full[s]);
       }
     }
@@ -184,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % ST;
         if (!mbar_wait(&v_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x20c)) break;
-        const int col = list[j];
+        const int col = lst[j];
         const int ia = infoA[col], ib = infoB[col];
         mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES + (ia >= 0 ? 512 : 0) + (ib >= 0 ? 512 : 0));
 #pragma unroll
@@ -246,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1, st = j % ST;
-      const int inf = info[list[j]];  // the same for every row of this warp (one half per warp)
+      const int inf = info[lst[j]];  // the same for every row of this warp (one half per warp)
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, A.err, 0x207)) { ok = false; break; }
       tc_fence_after();
       float s[64];
@@ -321,26 +344,49 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (ok && ntiles > 0) ok = mbar_wait(&s_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.err, 0x209);
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(A.o) + (bh * A.Lq + row) * (int64_t)D;
+    const float row_lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    if (n_split == 1) {
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(A.o) + (bh * A.Lq + row) * (int64_t)D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      float o[32];
-      if (ntiles > 0) {
-        tmem_ld32_sync(t_row + Cfg::O_COL + c0, o);
-      } else {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        if (ntiles > 0) {
+          tmem_ld32_sync(t_row + Cfg::O_COL + c0, o);
+        } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] = 0.f;
-      }
-      if (row < A.Lq) {
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+        if (row < A.Lq) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 8) {
-          uint4 w = make_uint4(pack_bf16x2(o[x] * inv, o[x + 1] * inv), pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv),
-                               pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv), pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv));
-          *reinterpret_cast<uint4*>(orow + c0 + x) = w;
+          for (int x = 0; x < 32; x += 8) {
+            uint4 w = make_uint4(pack_bf16x2(o[x] * inv, o[x + 1] * inv), pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv),
+                                 pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv), pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv));
+            *reinterpret_cast<uint4*>(orow + c0 + x) = w;
+          }
         }
       }
+      if (row < A.Lq && A.lse) A.lse[bh * A.Lq + row] = row_lse;
+    } else {
+      // normalised fp32 partial of this chunk and its LSE (an empty chunk gives 0 and -inf)
+      const int64_t prow = (int64_t)y * A.Lq + row;
+      float* po = P.part_o + prow * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        if (ntiles > 0) {
+          tmem_ld32_sync(t_row + Cfg::O_COL + c0, o);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0.f;
+        }
+        if (row < A.Lq) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 4)
+            *reinterpret_cast<float4*>(po + c0 + x) = make_float4(o[x] * inv, o[x + 1] * inv, o[x + 2] * inv, o[x + 3] * inv);
+        }
+      }
+      if (row < A.Lq) P.part_lse[prow] = row_lse;
     }
-    if (row < A.Lq && A.lse) A.lse[bh * A.Lq + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
@@ -348,6 +394,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
+}
+
+// Log-sum-exp merge of the chunks of split heads: one warp per (rank, batch, query
+// row); O (bf16) and LSE go to the caller's arrays.
+template <int D>
+__global__ void __launch_bounds__(256) mha_split_merge_kernel(const MhaArgs A, const MhaSplit P) {
+  constexpr int E = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= A.Lq) return;
+  const int rank = blockIdx.y / A.B, bi = blockIdx.y - rank * A.B;
+  const int ns = P.uniform_s > 0 ? P.uniform_s : P.s[rank];
+  const int y0 = (P.uniform_s > 0 ? rank * A.B * ns : P.ybase[rank]) + bi * ns;
+  const int64_t pr = (int64_t)y0 * A.Lq + row;
+  float out[E];
+  const float L = merge_row<E>(P.part_o + pr * D, (size_t)A.Lq * D, P.part_lse + pr, (size_t)A.Lq, ns, lane, out);
+  const int64_t orow = ((int64_t)bi * A.H + A.hmap.order[rank]) * A.Lq + row;
+  __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + orow * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(op + e) = pack_bf16x2(out[e], out[e + 1]);
+  if (A.lse && lane == 0) A.lse[orow] = L;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -376,7 +443,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int d, int L, int BH, int rows)
 }
 
 template <int D>
-sta_status launch_t(const MhaArgs& a, cudaStream_t st) {
+sta_status launch_t(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   const int BH = a.B * a.H;
   if (!make_tmap(&tq, a.q, D, a.Lq, BH, kBM) || !make_tmap(&tk, a.k, D, a.Lk, BH, kBN) ||
@@ -387,9 +454,14 @@ sta_status launch_t(const MhaArgs& a, cudaStream_t st) {
   const size_t smem = blk_smem_bytes<D>(a.mask.ot_cols);
   auto kern = mha_block_kernel<D>;
   STA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  const dim3 grid((unsigned)cdiv(a.Lq, kBM), (unsigned)BH);
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  const dim3 grid((unsigned)cdiv(a.Lq, kBM), (unsigned)p.n_y);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a, p);
   STA_LAUNCH_CHECK();
+  if (p.n_split_ranks > 0) {
+    const dim3 mgrid((unsigned)cdiv(a.Lq, 8), (unsigned)(p.n_split_ranks * a.B));
+    mha_split_merge_kernel<D><<<mgrid, 256, 0, st>>>(a, p);
+    STA_LAUNCH_CHECK();
+  }
   return STA_OK;
 }
 
@@ -399,9 +471,71 @@ bool block_kernel_supports(int d, int Lk, int dtype) {
   return dtype == STA_BF16 && (d == 64 || d == 128) && cdiv(Lk, 64) <= kMaxCols;
 }
 
-sta_status launch_mha_block(const MhaArgs& a, cudaStream_t st) {
+sta_status launch_mha_block(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {
   if (!block_kernel_supports(a.d, a.Lk, a.dtype)) return STA_ERR_UNSUPPORTED;
-  return a.d == 64 ? launch_t<64>(a, st) : launch_t<128>(a, st);
+  if (p.n_split_ranks > 0 && (!p.part_o || !p.part_lse)) return STA_ERR_WORKSPACE;
+  return a.d == 64 ? launch_t<64>(a, p, st) : launch_t<128>(a, p, st);
+}
+
+// Split planner. Without an explicit count, the work of an item is its key
+// tiles plus kSetupTiles for the prologue (union build, first loads) and
+// epilogue; an item longer than the average work of a resident CTA slot (two
+// per SM) by more than a factor of two would outlast the rest of the grid, so it
+// is cut into chunks of about that length (at least kMinChunk tiles). Shorter
+// items stay whole: a chunk costs another prologue and a merged partial.
+sta_status plan_mha_split(const MhaArgs& a, const int64_t* mask_head_tiles, int num_splits, int device, MhaSplit& p) {
+  constexpr int kMinChunk = 16;
+  constexpr int kMaxAutoSplit = 32;
+  constexpr double kSetupTiles = 4.0;
+  const int H = a.H, B = a.B;
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
+  if (num_splits > 0) {
+    for (int r = 0; r < H; ++r) p.s[r] = (uint16_t)num_splits;
+  } else if (!mask_head_tiles) {
+    for (int r = 0; r < H; ++r) p.s[r] = 1;
+  } else {
+    int sms = 0;
+    if (device < 0) STA_CUDA_TRY(cudaGetDevice(&device));
+    STA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+    const int64_t nqt = cdiv(a.Lq, kBM);
+    const int R = a.mask.ot_rows;
+    double w[kMaxHeads], W = 0.0;
+    for (int r = 0; r < H; ++r) {
+      // key tiles of one 128-row item ~ the mask head's non-empty tiles per outer-tile row
+      w[r] = (double)cdiv(mask_head_tiles[a.hmap.m[a.hmap.order[r]]], R);
+      W += (double)B * (double)nqt * (w[r] + kSetupTiles);
+    }
+    const double target = fmax((double)kMinChunk, W / (2.0 * (double)(sms > 0 ? sms : 1)));
+    for (int r = 0; r < H; ++r) {
+      // an item within twice the target still ends in time: only longer ones are cut
+      int sr = w[r] > 2.0 * target ? (int)ceil(w[r] / target) : 1;
+      sr = sr < 1 ? 1 : (sr > kMaxAutoSplit ? kMaxAutoSplit : sr);
+      if (r > 0 && sr > p.s[r - 1]) sr = p.s[r - 1];  // split ranks stay a prefix of the launch order
+      p.s[r] = (uint16_t)sr;
+    }
+  }
+  int64_t y = 0;
+  p.n_split_ranks = 0;
+  bool uniform = true;
+  for (int r = 0; r < H; ++r) {
+    p.ybase[r] = (int32_t)y;
+    y += (int64_t)B * p.s[r];
+    if (y > 65535) return STA_ERR_UNSUPPORTED;  // grid.y limit
+    if (p.s[r] > 1) p.n_split_ranks = r + 1;
+    uniform = uniform && p.s[r] == p.s[0];
+  }
+  p.ybase[H] = (int32_t)y;
+  p.n_y = (int)y;
+  p.uniform_s = uniform ? p.s[0] : 0;
+  return STA_OK;
+}
+
+size_t mha_split_workspace_bytes(const MhaArgs& a, const MhaSplit& p) {
+  if (p.n_split_ranks == 0) return 0;
+  const size_t rows = (size_t)p.ybase[p.n_split_ranks] * (size_t)a.Lq;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return al(rows * (size_t)a.d * sizeof(float)) + al(rows * sizeof(float));
 }
 
 }  // namespace sta

@@ -139,3 +139,35 @@ def test_merge_rejects_bad_arguments_on_host(lib):
     assert lib.sta_merge_lse(P, P, 4, 2, 64, P, 7, None, None) == sta.STA_ERR_INVALID_ARG
     assert lib.sta_merge_lse(None, P, 4, 2, 64, P, 0, None, None) == sta.STA_ERR_INVALID_ARG
     assert lib.sta_merge_lse(None, None, 0, 2, 64, None, 0, None, None) == sta.STA_OK
+
+
+def _mha_split(lib, splits, B=1, H=2, Lq=128, d=64, ws=None, ws_bytes=0, kernel=0, dtype=sta.STA_BF16):
+    m = _mask_struct(Lq=Lq, Lk=Lq)
+    n = C.c_size_t(ws_bytes)
+    st = lib.sta_mha_fwd_splitkv(16, 16, 16, 16, None, C.byref(m), None, B, H, Lq, Lq, d, dtype, 0.125, kernel,
+                                 splits, ws, C.byref(n), None)
+    return st, n.value
+
+
+def test_mha_splitkv_workspace_query_on_host(lib):
+    # s chunks for every (b, h): partial rows = B * H * s * Lq, d floats + one LSE each
+    st, n = _mha_split(lib, 4)
+    rows = 1 * 2 * 4 * 128
+    assert st == sta.STA_OK and n == rows * 64 * 4 + rows * 4
+    st, n = _mha_split(lib, 3, Lq=100, d=128)
+    rows = 2 * 3 * 100
+    assert st == sta.STA_OK and n == ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert _mha_split(lib, 1) == (sta.STA_OK, 256)  # nothing split: the minimum
+    assert _mha_split(lib, 0) == (sta.STA_OK, 256)  # no tile counts in the mask: no split
+    assert _mha_split(lib, 4, kernel=sta.STA_KERNEL_ROW) == (sta.STA_OK, 256)  # the row kernel runs unsplit
+    assert _mha_split(lib, -1)[0] == sta.STA_ERR_INVALID_ARG
+    assert _mha_split(lib, 1025)[0] == sta.STA_ERR_INVALID_ARG
+    assert _mha_split(lib, 1024, B=64, H=2)[0] == sta.STA_ERR_UNSUPPORTED  # grid.y above 65535
+    assert _mha_split(lib, 4, ws=C.c_void_p(256), ws_bytes=1000)[0] == sta.STA_ERR_WORKSPACE
+    assert _mha_split(lib, 4, ws=C.c_void_p(272), ws_bytes=1 << 20)[0] == sta.STA_ERR_UNSUPPORTED  # alignment
+    m = _mask_struct()
+    n = C.c_size_t(0)
+    assert lib.sta_mha_fwd_splitkv(16, 16, 16, 16, None, C.byref(m), None, 1, 2, 128, 128, 64, sta.STA_BF16, 0.125,
+                                   0, 2, None, None, None) == sta.STA_ERR_INVALID_ARG  # no size pointer
+    assert lib.sta_mha_fwd_splitkv(16, 16, 16, 16, None, C.byref(m), None, 1, 2, 128, 128, 96, sta.STA_BF16, 0.125,
+                                   0, 2, None, C.byref(n), None) == sta.STA_ERR_UNSUPPORTED
