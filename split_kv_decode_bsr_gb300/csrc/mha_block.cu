@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kBM = 128;       // query rows per CTA
 constexpr int kBN = 64;        // keys per tile (one outer tile)
-constexpr int kThreads = 224;  // warp 0 K loads, warp 1 MMA, warps 2..5 softmax, warp 6 V loads
+constexpr int kThreads = 256;  // warp 0 K loads, warp 1 QK MMAs, warps 2..5 softmax, warp 6 V loads, warp 7 PV MMAs
 constexpr int kMaxCols = 1024; // outer-tile columns supported (Lk <= 65536)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -44,6 +44,10 @@ template <int D>
 struct BlkCfg {
   static constexpr int KH = D / 64;                 // 128-byte column blocks of a row
   static constexpr int STAGES = D == 64 ? 5 : 2;
+  // With two stages the K and V rings move in step with the S/P buffers: stage j & 1 is
+  // free again exactly when QK(j) (K) or PV(j) (V) has completed, so the loaders wait on
+  // s_full / pv_done and the MMA issuers commit once per tile instead of two or three times.
+  static constexpr bool PAIR_RING = STAGES == 2;
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = kBN * D * 2;      // one K or V tile
   static constexpr int OFF_Q = 0;
@@ -52,8 +56,14 @@ struct BlkCfg {
   static constexpr int OFF_BM = OFF_V + STAGES * KV_BYTES;  // per stage: part bitmaps of both halves (2 x 512 B)
   static constexpr int OFF_INFO = OFF_BM + STAGES * 1024;  // then infoA[C], infoB[C], list[C]
   static constexpr int TMEM_COLS = 256;
-  static constexpr int S_COL = 0;                   // S buffers at columns 0 and 64; P(j) over S(j)'s first 32
-  static constexpr int O_COL = 128;
+  // TMEM columns: S buffers at 0 and 64. With d = 64 there is room for P buffers of their
+  // own (columns 128 and 160) and O at 192, so that an S buffer is free again as soon as
+  // the softmax has read it; with d = 128, O takes columns 128..255 and P(j) is written
+  // over the first 32 columns of S(j), which then stays busy until PV(j) has completed.
+  static constexpr bool SEP_P = D == 64;
+  static constexpr int S_COL = 0;
+  static constexpr int P_COL = SEP_P ? 128 : 0;
+  static constexpr int O_COL = SEP_P ? 192 : 128;
   static constexpr uint32_t IDESC_QK = umma_idesc_bf16(kBM, kBN, 0, 0);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kBM, D, 0, 1);
 };
@@ -67,18 +77,22 @@ size_t blk_smem_bytes(int C) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     mha_block_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const MhaArgs A, const MhaSplit P) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const MhaArgs A, const MhaSplit P) {
   using Cfg = BlkCfg<D>;
   constexpr int ST = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  // Per S/P buffer b (tile j uses b = j & 1): s_full[b] S(j) is in TMEM; p_full[b] P(j) is in TMEM
-  // (all 128 softmax threads); s_free[b] PV(j) has completed (committed by the MMA warp).
+  // Per buffer b (tile j uses b = j & 1): s_full[b] S(j) is in TMEM; p_full[b] P(j) is in TMEM
+  // (all 128 softmax threads); pv_done[b] PV(j) has completed (committed by the MMA warp);
+  // s_free[b] the S buffer may be overwritten: read by all 128 softmax threads (separate P
+  // buffers) or PV(j) completed (P over S).
   // K stage s is released as soon as its QK has completed (k_empty), V stage s (with the
   // part-tile bitmaps, which the softmax reads) once its PV has completed (v_empty).
   __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST], s_full[2], s_free[2],
-      p_full[2];
+      p_full[2], pv_done[2];
   __shared__ uint32_t s_tmem_base;
-  __shared__ int s_ntiles, s_jb;
+  __shared__ int s_rowptr[8];         // full/part row_ptr pairs of outer-tile rows 2qt and 2qt+1
+  __shared__ uint32_t s_colbits[32];  // bit c: column c is non-empty in either row (C <= 1024)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x;
@@ -114,6 +128,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint16_t* list = reinterpret_cast<uint16_t*>(infoB + C);
 
   // ---- setup: barriers, TMEM, union of the two outer-tile rows' columns
+  // The row pointers are fetched first; their latency overlaps the barrier and TMEM setup.
+  int rp = 0;
+  if (threadIdx.x < 8) {
+    const int a = 2 * qt + (threadIdx.x >> 2);  // threads 0..3: row 2qt, 4..7: row 2qt+1
+    if (a < R) {
+      const int64_t r = (int64_t)hm * R + a + (threadIdx.x & 1);
+      rp = (threadIdx.x & 2) ? A.mask.part_row_ptr[r] : A.mask.full_row_ptr[r];
+    }
+  }
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
     for (int s = 0; s < ST; ++s) {
@@ -124,8 +147,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 1);
+      mbar_init(&s_free[s], Cfg::SEP_P ? 128 : 1);
       mbar_init(&p_full[s], 128);
+      mbar_init(&pv_done[s], 1);
     }
     fence_mbar_init();
   }
@@ -137,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     infoA[c] = kEmpty;
     infoB[c] = kEmpty;
   }
+  if (threadIdx.x < 8) s_rowptr[threadIdx.x] = rp;
   __syncthreads();
   // Q does not depend on the column union: start its load now, under the union's latency.
   if (threadIdx.x == 0) {
@@ -149,39 +174,47 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_load_3d(smem + Cfg::OFF_Q + kh * (kBM * 128), &tm_q, kh * 64, qt * kBM, (int)bh, &q_full);
   }
   {
-    const int a0 = 2 * qt, a1 = 2 * qt + 1;
-    const int64_t rA = (int64_t)hm * R + a0, rB = (int64_t)hm * R + a1;
-    const bool hasB = a1 < R;
-    const int fA0 = A.mask.full_row_ptr[rA], fA1 = A.mask.full_row_ptr[rA + 1];
-    const int pA0 = A.mask.part_row_ptr[rA], pA1 = A.mask.part_row_ptr[rA + 1];
-    const int fB0 = hasB ? A.mask.full_row_ptr[rB] : 0, fB1 = hasB ? A.mask.full_row_ptr[rB + 1] : 0;
-    const int pB0 = hasB ? A.mask.part_row_ptr[rB] : 0, pB1 = hasB ? A.mask.part_row_ptr[rB + 1] : 0;
+    const int fA0 = s_rowptr[0], fA1 = s_rowptr[1], pA0 = s_rowptr[2], pA1 = s_rowptr[3];
+    const int fB0 = s_rowptr[4], fB1 = s_rowptr[5], pB0 = s_rowptr[6], pB1 = s_rowptr[7];
     for (int t = fA0 + threadIdx.x; t < fA1; t += kThreads) infoA[A.mask.full_col_idx[t]] = kFull;
     for (int t = pA0 + threadIdx.x; t < pA1; t += kThreads) infoA[A.mask.part_col_idx[t]] = t;
     for (int t = fB0 + threadIdx.x; t < fB1; t += kThreads) infoB[A.mask.full_col_idx[t]] = kFull;
     for (int t = pB0 + threadIdx.x; t < pB1; t += kThreads) infoB[A.mask.part_col_idx[t]] = t;
   }
   __syncthreads();
-  if (warp == 0) {
-    int n = 0;
-    for (int c0 = 0; c0 < C; c0 += 32) {
-      const int c = c0 + lane;
-      const bool ne = c < C && (infoA[c] != kEmpty || infoB[c] != kEmpty);
-      const unsigned b = __ballot_sync(0xffffffffu, ne);
-      if (ne) list[n + __popc(b & ((1u << lane) - 1u))] = (uint16_t)c;
-      n += __popc(b);
+  // Ascending list of the non-empty columns, built by all warps: one ballot per 32 columns,
+  // a prefix over the (at most 32) words, then every set bit written at its rank.
+  const int nwords = (C + 31) >> 5;
+  int n_cols;  // size of the union (every thread computes it)
+  for (int wd = warp; wd < nwords; wd += kThreads / 32) {
+    const int c = wd * 32 + lane;
+    const unsigned b = __ballot_sync(0xffffffffu, c < C && (infoA[c] != kEmpty || infoB[c] != kEmpty));
+    if (lane == 0) s_colbits[wd] = b;
+  }
+  __syncthreads();
+  {
+    const unsigned wl = lane < nwords ? s_colbits[lane] : 0u;
+    int incl = __popc(wl);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
-    if (lane == 0) {  // this CTA's chunk of the column list
-      const int jb = (int)((int64_t)chunk * n / n_split);
-      s_jb = jb;
-      s_ntiles = (int)((int64_t)(chunk + 1) * n / n_split) - jb;
+    const int excl = incl - __popc(wl);
+    for (int wd = warp; wd < nwords; wd += kThreads / 32) {
+      const unsigned b = __shfl_sync(0xffffffffu, wl, wd);
+      const int base = __shfl_sync(0xffffffffu, excl, wd);
+      if ((b >> lane) & 1u) list[base + __popc(b & ((1u << lane) - 1u))] = (uint16_t)(wd * 32 + lane);
     }
+    n_cols = __shfl_sync(0xffffffffu, incl, 31);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int ntiles = s_ntiles;
-  const uint16_t* lst = list + s_jb;
+  // this CTA's chunk of the column list (n_cols <= 1024, n_split <= 1024: no overflow)
+  const int jb = chunk * n_cols / n_split;
+  const int ntiles = (chunk + 1) * n_cols / n_split - jb;
+  const uint16_t* lst = list + jb;
   const uint32_t tmem = s_tmem_base;
   const uint32_t sQ = smem_u32(smem + Cfg::OFF_Q);
   const uint32_t sK = smem_u32(smem + Cfg::OFF_K);
@@ -193,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0 && ntiles > 0) {
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % ST;
-        if (!mbar_wait(&k_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x201)) break;
+        if (!mbar_wait(Cfg::PAIR_RING ? &s_full[s] : &k_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x201)) break;
         mbar_arrive_expect_tx(&k_full[s], Cfg::KV_BYTES);
 #pragma unroll
         for (int kh = 0; kh < Cfg::KH; ++kh)
@@ -206,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0 && ntiles > 0) {
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % ST;
-        if (!mbar_wait(&v_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x20c)) break;
+        if (!mbar_wait(Cfg::PAIR_RING ? &pv_done[s] : &v_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x20c)) break;
         const int col = lst[j];
         const int ia = infoA[col], ib = infoB[col];
         mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES + (ia >= 0 ? 512 : 0) + (ib >= 0 ? 512 : 0));
@@ -221,41 +254,49 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK MMA issuer
+    // (a tcgen05.mma costs its issuing thread ~60 cycles: QK and PV are issued by two
+    // threads so that their issue latencies overlap)
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&q_full, 0, A.err, 0x202);
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j % ST, sb = j & 1;
-        if (!mbar_wait(&p_full[sb], (j >> 1) & 1, A.err, 0x203)) return false;
-        if (!mbar_wait(&v_full[s], (j / ST) & 1, A.err, 0x204)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd = umma_sdesc_sw128(sV + s * Cfg::KV_BYTES + kk * 2048, kBN * 128, 1024);
-          umma_bf16_ts(tmem + Cfg::O_COL, tmem + Cfg::S_COL + sb * kBN + kk * 8, bd, Cfg::IDESC_PV,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&v_empty[s]);
-        umma_commit(&s_free[sb]);
-        return true;
-      };
+      // descriptors of Q and of K stage 0; every other operand is a fixed offset from them
+      const uint64_t a0 = umma_sdesc_sw128(sQ, 16, 1024), b0 = umma_sdesc_sw128(sK, 16, 1024);
+      uint64_t* s_reuse = Cfg::SEP_P ? s_free : (Cfg::PAIR_RING ? pv_done : s_free);
       for (int j = 0; ok && j < ntiles; ++j) {
         const int s = j % ST, sb = j & 1;
-        if (!mbar_wait(&k_full[s], (j / ST) & 1, A.err, 0x205)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&s_free[sb], ((j - 2) >> 1) & 1, A.err, 0x206)) { ok = false; break; }
+        if (!mbar_wait(&k_full[s], (j / ST) & 1, A.err, 0x205)) break;
+        if (j >= 2 && !mbar_wait(&s_reuse[sb], ((j - 2) >> 1) & 1, A.err, 0x206)) break;
         tc_fence_after();
+        const uint64_t bs = b0 + (uint64_t)((s * Cfg::KV_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int kh = kk >> 2, ko = (kk & 3) * 32;
-          const uint64_t ad = umma_sdesc_sw128(sQ + kh * (kBM * 128) + ko, 16, 1024);
-          const uint64_t bd = umma_sdesc_sw128(sK + s * Cfg::KV_BYTES + kh * (kBN * 128) + ko, 16, 1024);
-          umma_bf16(tmem + Cfg::S_COL + sb * kBN, ad, bd, Cfg::IDESC_QK, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem + Cfg::S_COL + sb * kBN, a0 + (uint64_t)((kh * (kBM * 128) + ko) >> 4),
+                    bs + (uint64_t)((kh * (kBN * 128) + ko) >> 4), Cfg::IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[sb]);
-        umma_commit(&k_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (!Cfg::PAIR_RING) umma_commit(&k_empty[s]);
       }
-      if (ok) issue_pv(ntiles - 1);
+    }
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ PV MMA issuer
+    if (lane == 0) {
+      const uint64_t v0 = umma_sdesc_sw128(sV, kBN * 128, 1024);
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % ST, sb = j & 1;
+        if (!mbar_wait(&p_full[sb], (j >> 1) & 1, A.err, 0x203)) break;
+        if (!mbar_wait(&v_full[s], (j / ST) & 1, A.err, 0x204)) break;
+        tc_fence_after();
+        const uint64_t vs = v0 + (uint64_t)((s * Cfg::KV_BYTES) >> 4);
+        const uint32_t p_tmem = Cfg::SEP_P ? tmem + Cfg::P_COL + sb * 32 : tmem + Cfg::S_COL + sb * kBN;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_bf16_ts(tmem + Cfg::O_COL, p_tmem + kk * 8, vs + (uint64_t)((kk * 2048) >> 4), Cfg::IDESC_PV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        if (!Cfg::PAIR_RING) umma_commit(&v_empty[s]);
+        umma_commit(&pv_done[sb]);
+        if (!Cfg::SEP_P && !Cfg::PAIR_RING) umma_commit(&s_free[sb]);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -274,6 +315,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc_fence_after();
       float s[64];
       tmem_ld64_sync(t_row + Cfg::S_COL + sb * kBN, s);
+      if (Cfg::SEP_P) {  // S(j) is in registers: its buffer may take S(j+2)
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
+      }
       uint32_t pk[32];
       float alpha = 1.f;
       bool need = false;
@@ -322,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       }
       if (__any_sync(0xffffffffu, need)) {
-        // O may only be rescaled once PV(j-1) has completed (its buffer's s_free phase)
-        if (j >= 1 && !mbar_wait(&s_free[(j - 1) & 1], ((j - 1) >> 1) & 1, A.err, 0x208)) { ok = false; break; }
+        // O may only be rescaled once PV(j-1) has completed
+        if (j >= 1 && !mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, A.err, 0x208)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -334,19 +379,31 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st32_sync(t_row + Cfg::O_COL + c0, reinterpret_cast<const uint32_t*>(o));
         }
       }
-      // P(j), bf16 pairs, over the first 32 columns of S(j) (already in registers)
-      tmem_st32_sync(t_row + Cfg::S_COL + sb * kBN, pk);
+      if (Cfg::SEP_P) {
+        // P(j), bf16 pairs, into P buffer j & 1 once PV(j-2) has read it
+        if (j >= 2 && !mbar_wait(&pv_done[sb], ((j - 2) >> 1) & 1, A.err, 0x20e)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st32_sync(t_row + Cfg::P_COL + sb * 32, pk);
+      } else {
+        // P(j), bf16 pairs, over the first 32 columns of S(j) (already in registers)
+        tmem_st32_sync(t_row + Cfg::S_COL + sb * kBN, pk);
+      }
       tc_fence_before();
       mbar_arrive(&p_full[sb]);
     }
     // ---- epilogue: O / l (bf16) and LSE
     const int row = qt * kBM + m;
-    if (ok && ntiles > 0) ok = mbar_wait(&s_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.err, 0x209);
+    if (ok && ntiles > 0) ok = mbar_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.err, 0x209);
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float row_lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     if (n_split == 1) {
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(A.o) + (bh * A.Lq + row) * (int64_t)D;
+      // O / l as bf16 into the Q buffer (idle once the last QK has completed), in the
+      // 128-byte-swizzled layout of the O tensor map, then one TMA store per 64 columns;
+      // rows past Lq fall outside the tensor map and are not written.
+      uint8_t* so = smem + Cfg::OFF_Q;
+      // with no tile the Q load may still be landing in that buffer
+      if (ntiles == 0 && !mbar_wait(&q_full, 0, A.err, 0x20d)) ok = false;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
@@ -356,16 +413,23 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = 0.f;
         }
-        if (row < A.Lq) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 8) {
-            uint4 w = make_uint4(pack_bf16x2(o[x] * inv, o[x + 1] * inv), pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv),
-                                 pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv), pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv));
-            *reinterpret_cast<uint4*>(orow + c0 + x) = w;
-          }
+        for (int x = 0; x < 32; x += 8) {
+          const uint4 w = make_uint4(pack_bf16x2(o[x] * inv, o[x + 1] * inv), pack_bf16x2(o[x + 2] * inv, o[x + 3] * inv),
+                                     pack_bf16x2(o[x + 4] * inv, o[x + 5] * inv), pack_bf16x2(o[x + 6] * inv, o[x + 7] * inv));
+          const int kh = c0 >> 6, q16 = ((c0 & 63) + x) >> 3;  // 16-byte chunk within the 128-byte row
+          *reinterpret_cast<uint4*>(so + kh * (kBM * 128) + m * 128 + ((q16 ^ (m & 7)) << 4)) = w;
         }
       }
       if (row < A.Lq && A.lse) A.lse[bh * A.Lq + row] = row_lse;
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (m == 0) {
+#pragma unroll
+        for (int kh = 0; kh < Cfg::KH; ++kh) tma_store_3d(&tm_o, so + kh * (kBM * 128), kh * 64, qt * kBM, (int)bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // shared memory is released when the CTA exits
+      }
     } else {
       // normalised fp32 partial of this chunk and its LSE (an empty chunk gives 0 and -inf)
       const int64_t prow = (int64_t)y * A.Lq + row;
@@ -444,10 +508,10 @@ bool make_tmap(CUtensorMap* m, const void* base, int d, int L, int BH, int rows)
 
 template <int D>
 sta_status launch_t(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int BH = a.B * a.H;
   if (!make_tmap(&tq, a.q, D, a.Lq, BH, kBM) || !make_tmap(&tk, a.k, D, a.Lk, BH, kBN) ||
-      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN)) {
+      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN) || !make_tmap(&to, a.o, D, a.Lq, BH, kBM)) {
     note_cuda_error(cudaErrorInvalidValue);  // tensor-map encoding refused
     return STA_ERR_CUDA;
   }
@@ -455,7 +519,7 @@ sta_status launch_t(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {
   auto kern = mha_block_kernel<D>;
   STA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   const dim3 grid((unsigned)cdiv(a.Lq, kBM), (unsigned)p.n_y);
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, a, p);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, to, a, p);
   STA_LAUNCH_CHECK();
   if (p.n_split_ranks > 0) {
     const dim3 mgrid((unsigned)cdiv(a.Lq, 8), (unsigned)(p.n_split_ranks * a.B));

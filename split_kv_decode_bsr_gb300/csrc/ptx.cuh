@@ -53,18 +53,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that suspends the thread until the phase completes or about `hint_ns`
+// have passed, so that a waiting warp takes no issue slots from its neighbours.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendHintNs = 1000000u;  // 1 ms per try: the time limit is checked between tries
+
 // Wait for the phase with the given parity to complete; false after the time limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int err_code) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        record_error(err, err_code);
-        return false;
-      }
-      __nanosleep(64);
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(err, err_code);
+      return false;
     }
   }
 }
@@ -94,6 +104,22 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, in
       "[%6];" ::"r"(smem_u32(smem_dst)),
       "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+// Tiled tensor store (TMA) shared -> global of a 3-D box, tracked by the bulk-group
+// mechanism; parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+               "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(smem_src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Barrier over `count` threads (a multiple of 32) on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
@@ -157,6 +183,8 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, i
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (layout code 2), descriptor version 1.
+// The start address sits in bits 0..13 (address >> 4): for a shared address below 256 KB
+// a byte offset off (multiple of 16) moves it by adding off >> 4 to the descriptor.
 __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
