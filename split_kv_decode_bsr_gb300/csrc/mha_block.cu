@@ -334,19 +334,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t lo = (uint32_t)bits, hi = (uint32_t)(bits >> 32);
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
-            s[x] = ((lo >> x) & 1u) ? s[x] : -INFINITY;
-            s[x + 32] = ((hi >> x) & 1u) ? s[x + 32] : -INFINITY;
+            s[x] = (lo & (1u << x)) ? s[x] : -INFINITY;
+            s[x + 32] = (hi & (1u << x)) ? s[x + 32] : -INFINITY;
           }
         }
         float m8[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) m8[x] = fmaxf(s[x], s[x + 8]);
-#pragma unroll
-        for (int x = 16; x < 64; x += 8)
-#pragma unroll
-          for (int y = 0; y < 8; ++y) m8[y] = fmaxf(m8[y], s[x + y]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * c;
+        for (int y = 0; y < 8; ++y) {
+          m8[y] = fmax3(s[y], s[y + 8], s[y + 16]);
+          m8[y] = fmax3(m8[y], s[y + 24], s[y + 32]);
+          m8[y] = fmax3(m8[y], s[y + 40], s[y + 48]);
+          m8[y] = fmaxf(m8[y], s[y + 56]);
+        }
+        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c;
         if (mx > m_ref + kRescaleThreshold) {
           if (m_ref != -INFINITY) {
             alpha = ex2(m_ref - mx);
@@ -355,16 +355,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           m_ref = mx;
         }
         const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-        float l8[8];
+        // exponent arguments and the row sum on packed fp32 pairs (one instruction per pair)
+        const uint64_t c2 = f32x2_pack(c, c), nm2 = f32x2_pack(neg_m, neg_m);
+        uint64_t l2[4];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) l8[x] = 0.f;
+        for (int x = 0; x < 4; ++x) l2[x] = 0ull;
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const float p0 = ex2(fmaf(s[2 * x], c, neg_m)), p1 = ex2(fmaf(s[2 * x + 1], c, neg_m));
-          l8[x & 7] += p0 + p1;
+          float a0, a1;
+          f32x2_unpack(f32x2_fma(f32x2_pack(s[2 * x], s[2 * x + 1]), c2, nm2), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          l2[x & 3] = f32x2_add(l2[x & 3], f32x2_pack(p0, p1));
           pk[x] = pack_bf16x2(p0, p1);
         }
-        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        float lp[8];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) f32x2_unpack(l2[x], lp[2 * x], lp[2 * x + 1]);
+        l = l * alpha + (((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7])));
       }
       if (__any_sync(0xffffffffu, need)) {
         // O may only be rescaled once PV(j-1) has completed
