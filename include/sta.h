@@ -98,7 +98,28 @@ typedef struct {
    * there, and sta_mha_fwd then starts the query tiles of the heaviest heads
    * first (load balance); results do not depend on it. */
   int64_t* head_tiles;
+  /* Optional DEVICE buffer of sta_tile_lists_bytes(Hm, Lq, Lk) bytes (caller-
+   * owned, 16-byte aligned) or NULL. When set, the fill call of sta_encode_mask
+   * also writes the column lists of the block-wise kernel there, and
+   * sta_mha_fwd / sta_mha_fwd_splitkv then read the list of each 128-row query
+   * tile with one copy instead of merging its two outer-tile rows themselves;
+   * results do not depend on it. Layout: T = ceil(ot_rows / 2) query tiles per
+   * mask head, Cp = ot_cols rounded up to a multiple of 8, one slot of
+   * 16 + 10 * Cp bytes per (hm, t) at slot index hm * T + t:
+   *   int32 n, 12 zero bytes          number of entries
+   *   uint16 col[Cp]                  ascending OT columns non-empty in OT row
+   *                                   2t or 2t+1 (entries >= n undefined)
+   *   int32 kind_a[Cp], kind_b[Cp]    per entry, for OT rows 2t and 2t+1: -1
+   *                                   empty, -2 full, >= 0 index of the part
+   *                                   tile (row 2t+1 beyond ot_rows is empty)
+   * Only for ot_cols <= 1024 (the block-wise kernel's limit). */
+  void* tile_lists;
 } sta_bsr_mask;
+
+/* Size in bytes of the tile_lists buffer for a mask of Hm heads over Lq x Lk
+ * (see sta_bsr_mask), or 0 when Hm, Lq or Lk is < 1 or ceil(Lk/64) > 1024.
+ * Host only. */
+size_t sta_tile_lists_bytes(int Hm, int Lq, int Lk);
 
 /* sta_encode_mask -- build the two-level mask from Hm sources
  * (STOF, 2 段階ストレージ形式).
@@ -121,7 +142,10 @@ typedef struct {
  *  3. Fill: all five device arrays set, out->n_full / n_part holding the
  *     capacities from a size query of the same mask. Writes everything,
  *     asynchronously. Entries beyond a capacity are never written.
- * Returns STA_ERR_INVALID_ARG for bad sizes, null pointers or kinds, and
+ *     With out->tile_lists set (ot_cols <= 1024), the per-query-tile column
+ *     lists are written as well.
+ * Returns STA_ERR_INVALID_ARG for bad sizes, null pointers or kinds (also for
+ * tile_lists with ot_cols > 1024 or not 16-byte aligned), and
  * STA_ERR_WORKSPACE if *workspace_bytes is below the requirement. */
 sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, int Lk, sta_bsr_mask* out, void* workspace,
                            size_t* workspace_bytes, sta_stream stream);

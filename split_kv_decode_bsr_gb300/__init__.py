@@ -36,7 +36,7 @@ STA_MASK_PATTERN, STA_MASK_DENSE_U8, STA_MASK_DENSE_BITS = 0, 1, 2
 STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
-EXPORTED = ("sta_encode_mask", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_select_kernel", "sta_decode_splitkv",
+EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_select_kernel", "sta_decode_splitkv",
             "sta_decode_splitkv_noalloc", "sta_merge_lse", "sta_status_string", "sta_device_error",
             "sta_last_cuda_error", "sta_last_cuda_error_string")
 
@@ -62,7 +62,7 @@ class _BsrMask(C.Structure):
                 ("ot_cols", C.c_int32), ("full_row_ptr", C.c_void_p), ("full_col_idx", C.c_void_p),
                 ("part_row_ptr", C.c_void_p), ("part_col_idx", C.c_void_p), ("part_bitmap", C.c_void_p),
                 ("n_full", C.c_int64), ("n_part", C.c_int64), ("n_valid", C.c_int64),
-                ("head_tiles", C.c_void_p)]
+                ("head_tiles", C.c_void_p), ("tile_lists", C.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -79,6 +79,8 @@ def lib():
             h = C.CDLL(LIB_PATH)
             P, i32, f32, sz = C.c_void_p, C.c_int, C.c_float, C.POINTER(C.c_size_t)
             h.sta_encode_mask.argtypes = [P, i32, i32, i32, C.POINTER(_BsrMask), P, sz, P]
+            h.sta_tile_lists_bytes.argtypes = [i32, i32, i32]
+            h.sta_tile_lists_bytes.restype = C.c_size_t
             h.sta_mha_fwd.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32, i32, P]
             h.sta_mha_fwd_splitkv.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32,
                                               i32, i32, P, sz, P]
@@ -93,7 +95,7 @@ def lib():
             h.sta_last_cuda_error_string.argtypes = []
             h.sta_last_cuda_error_string.restype = C.c_char_p
             for n in EXPORTED:
-                if n not in ("sta_status_string", "sta_last_cuda_error_string"):
+                if n not in ("sta_status_string", "sta_last_cuda_error_string", "sta_tile_lists_bytes"):
                     getattr(h, n).restype = C.c_int
             _lib_handle = h
     return _lib_handle
@@ -172,6 +174,7 @@ class BsrMask:
         self.part_bitmap = part_bitmap
         self.n_full, self.n_part, self.n_valid = n_full, n_part, n_valid
         self.head_tiles = None  # ctypes int64 array [Hm] when known
+        self.tile_lists = None  # uint8 device tensor of the block kernel's column lists, when encoded
 
     def struct(self) -> _BsrMask:
         s = _BsrMask()
@@ -183,6 +186,7 @@ class BsrMask:
         s.part_bitmap = self.part_bitmap.data_ptr() if self.n_part else None
         s.n_full, s.n_part, s.n_valid = self.n_full, self.n_part, self.n_valid
         s.head_tiles = C.cast(self.head_tiles, C.c_void_p) if self.head_tiles is not None else None
+        s.tile_lists = self.tile_lists.data_ptr() if self.tile_lists is not None else None
         return s
 
     def host_arrays(self) -> dict:
@@ -201,8 +205,19 @@ def _src_array(srcs: Sequence[MaskSource]):
     return arr
 
 
-def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, stream=None) -> BsrMask:
-    """Encode Hm = len(srcs) mask heads (size query, then fill). Synchronises once."""
+def tile_lists_bytes(Hm: int, Lq: int, Lk: int) -> int:
+    """Size of the block kernel's per-query-tile column lists (0 when Lk > 65536)."""
+    return int(lib().sta_tile_lists_bytes(Hm, Lq, Lk))
+
+
+def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, stream=None,
+                    tile_lists: bool = True) -> BsrMask:
+    """Encode Hm = len(srcs) mask heads (size query, then fill). Synchronises once.
+
+    tile_lists: also write the block kernel's per-query-tile column lists (when
+    the mask is narrow enough for them), which the MHA calls then copy instead of
+    building each tile's column union themselves.
+    """
     h = lib()
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     Hm = len(srcs)
@@ -224,9 +239,13 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
     pci = torch.empty(max(npart, 1), dtype=torch.int32, device=dev)
     pbm = torch.empty(max(npart, 1) * 64, dtype=torch.int64, device=dev)
     out.full_col_idx, out.part_col_idx, out.part_bitmap = fci.data_ptr(), pci.data_ptr(), pbm.data_ptr()
+    tl_bytes = int(h.sta_tile_lists_bytes(Hm, Lq, Lk)) if tile_lists else 0
+    tl = torch.empty(tl_bytes, dtype=torch.uint8, device=dev) if tl_bytes else None
+    out.tile_lists = tl.data_ptr() if tl is not None else None
     _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
     m = BsrMask(Hm, Lq, Lk, frp, fci[:nf], prp, pci[:npart], pbm[:npart * 64], nf, npart, nv)
     m.head_tiles = head_tiles
+    m.tile_lists = tl
     return m
 
 

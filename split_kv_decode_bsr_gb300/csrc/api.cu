@@ -138,7 +138,10 @@ sta_status mha_prepare(const sta_bsr_mask* mask, const int32_t* head_map, int B,
   which = kernel == STA_KERNEL_AUTO ? select_kernel(mask, d, Lk, dtype) : kernel;
   if (which == STA_KERNEL_BLOCK && !block_kernel_supports(d, Lk, dtype)) return STA_ERR_UNSUPPORTED;
   a.mask = MaskView{mask->full_row_ptr, mask->full_col_idx, mask->part_row_ptr, mask->part_col_idx,
-                    mask->part_bitmap, mask->ot_rows, mask->ot_cols};
+                    mask->part_bitmap, static_cast<const uint8_t*>(mask->tile_lists), mask->ot_rows, mask->ot_cols,
+                    mask->n_part};
+  if (mask->tile_lists && (mask->ot_cols > kMaxTileListCols || ((uintptr_t)mask->tile_lists & 15)))
+    return STA_ERR_INVALID_ARG;
   a.B = B; a.H = H; a.Lq = Lq; a.Lk = Lk; a.d = d; a.dtype = dtype;
   a.scale_log2 = scale * kLog2e;
   return STA_OK;

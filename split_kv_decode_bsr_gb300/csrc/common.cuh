@@ -32,6 +32,11 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+constexpr int kMaxTileListCols = 1024;  // OT columns the block-wise kernel (and its column lists) support
+
+// Size of the block-wise kernel's per-query-tile column lists (0 if not available).
+size_t tile_lists_bytes(int Hm, int Lq, int Lk);
+
 // Device copy of the encoded-mask arrays a kernel needs.
 struct MaskView {
   const int32_t* full_row_ptr;
@@ -39,7 +44,9 @@ struct MaskView {
   const int32_t* part_row_ptr;
   const int32_t* part_col_idx;
   const uint64_t* part_bitmap;
+  const uint8_t* tile_lists;  // optional, see sta_bsr_mask::tile_lists
   int32_t ot_rows, ot_cols;
+  int64_t n_part;              // part tiles (bounds the bitmap reads of the block-wise kernel)
 };
 
 // Row r (0..63) of a part outer tile: 64-bit key mask, bit c = column c of the tile.

@@ -4,7 +4,9 @@
 //
 // Three kernels per call: classify (one CTA per (mask head, OT row), warp-level
 // popcounts of the inner-tile words), a single-CTA scan of the per-row counts into
-// row_ptr, and fill (ballot-prefix positions, then the bitmaps of part tiles).
+// row_ptr, and fill (ballot-prefix positions, then the bitmaps of part tiles). When
+// the caller asks for them, a fourth kernel derives the block-wise kernel's column
+// lists (the union of the non-empty columns of each pair of OT rows) from the CSR.
 #include <vector>
 
 #include "common.cuh"
@@ -233,10 +235,79 @@ EncodeWs encode_ws_layout(int64_t Hm, int64_t R, int64_t C) {
   return w;
 }
 
+// Column lists of the block-wise kernel, one CTA per (query tile t, mask head):
+// the OT columns non-empty in row 2t or 2t+1, ascending, each with the kinds of
+// both rows (-1 empty, -2 full, part-tile index). Dynamic shared memory: two
+// int32 arrays of C (kind of each column per row). C <= 1024.
+__global__ void __launch_bounds__(256) encode_tile_lists_kernel(const int32_t* __restrict__ full_row_ptr,
+                                                                const int32_t* __restrict__ full_col_idx,
+                                                                const int32_t* __restrict__ part_row_ptr,
+                                                                const int32_t* __restrict__ part_col_idx, int R,
+                                                                int C, int Cp, uint8_t* __restrict__ lists) {
+  extern __shared__ int32_t kinds[];  // [2][C]
+  __shared__ uint32_t colbits[32];
+  const int t = blockIdx.x, hm = blockIdx.y, T = (R + 1) / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) kinds[c] = -1;
+  __syncthreads();
+  for (int half = 0; half < 2; ++half) {
+    const int a = 2 * t + half;
+    if (a >= R) continue;
+    const int64_t row = (int64_t)hm * R + a;
+    int32_t* k = kinds + half * C;
+    for (int i = full_row_ptr[row] + threadIdx.x; i < full_row_ptr[row + 1]; i += blockDim.x) k[full_col_idx[i]] = -2;
+    for (int i = part_row_ptr[row] + threadIdx.x; i < part_row_ptr[row + 1]; i += blockDim.x) k[part_col_idx[i]] = i;
+  }
+  __syncthreads();
+  const int nwords = (C + 31) >> 5;
+  for (int wd = warp; wd < nwords; wd += blockDim.x / 32) {
+    const int c = wd * 32 + lane;
+    const unsigned b = __ballot_sync(0xffffffffu, c < C && (kinds[c] != -1 || kinds[C + c] != -1));
+    if (lane == 0) colbits[wd] = b;
+  }
+  __syncthreads();
+  uint8_t* slot = lists + ((int64_t)hm * T + t) * (16 + 10 * (int64_t)Cp);
+  uint16_t* cols = reinterpret_cast<uint16_t*>(slot + 16);
+  int32_t* ka = reinterpret_cast<int32_t*>(slot + 16 + 2 * Cp);
+  int32_t* kb = ka + Cp;
+  const unsigned wl = lane < nwords ? colbits[lane] : 0u;
+  int incl = __popc(wl);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - __popc(wl);
+  for (int wd = warp; wd < nwords; wd += blockDim.x / 32) {
+    const unsigned b = __shfl_sync(0xffffffffu, wl, wd);
+    const int base = __shfl_sync(0xffffffffu, excl, wd);
+    const int c = wd * 32 + lane;
+    if ((b >> lane) & 1u) {
+      const int pos = base + __popc(b & ((1u << lane) - 1u));
+      cols[pos] = (uint16_t)c;
+      ka[pos] = kinds[c];
+      kb[pos] = kinds[C + c];
+    }
+  }
+  const int n = __shfl_sync(0xffffffffu, incl, 31);
+  if (threadIdx.x == 0) reinterpret_cast<int4*>(slot)[0] = make_int4(n, 0, 0, 0);
+}
+
 }  // namespace
+
+size_t tile_lists_bytes(int Hm, int Lq, int Lk) {
+  if (Hm < 1 || Lq < 1 || Lk < 1) return 0;
+  const int64_t R = cdiv(Lq, STA_OT), C = cdiv(Lk, STA_OT);
+  if (C > kMaxTileListCols) return 0;
+  const int64_t Cp = (C + 7) / 8 * 8;
+  return (size_t)Hm * (size_t)((R + 1) / 2) * (size_t)(16 + 10 * Cp);
+}
+
 }  // namespace sta
 
 using namespace sta;
+
+extern "C" size_t sta_tile_lists_bytes(int Hm, int Lq, int Lk) { return tile_lists_bytes(Hm, Lq, Lk); }
 
 extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, int Lk, sta_bsr_mask* out,
                                       void* workspace, size_t* workspace_bytes, sta_stream stream) {
@@ -268,6 +339,7 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
     if (out->n_full < 0 || out->n_part < 0) return STA_ERR_INVALID_ARG;
     if ((out->n_full > 0 && !out->full_col_idx) || (out->n_part > 0 && (!out->part_col_idx || !out->part_bitmap)))
       return STA_ERR_INVALID_ARG;
+    if (out->tile_lists && (C > kMaxTileListCols || ((uintptr_t)out->tile_lists & 15))) return STA_ERR_INVALID_ARG;
   }
   cudaStream_t st = (cudaStream_t)stream;
   char* ws = (char*)workspace;
@@ -334,6 +406,13 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
     encode_fill_kernel<<<dim3((unsigned)R, (unsigned)n), 256, 0, st>>>(
         make_batch(h0, n), Lq, Lk, (int)R, (int)C, cls, out->full_row_ptr, out->part_row_ptr, out->full_col_idx,
         out->part_col_idx, out->part_bitmap, out->n_full, out->n_part);
+    STA_LAUNCH_CHECK();
+  }
+  if (out->tile_lists) {
+    const int Cp = (int)((C + 7) / 8 * 8);
+    encode_tile_lists_kernel<<<dim3((unsigned)((R + 1) / 2), (unsigned)Hm), 256, 2 * C * sizeof(int32_t), st>>>(
+        out->full_row_ptr, out->full_col_idx, out->part_row_ptr, out->part_col_idx, (int)R, (int)C, Cp,
+        static_cast<uint8_t*>(out->tile_lists));
     STA_LAUNCH_CHECK();
   }
   return STA_OK;

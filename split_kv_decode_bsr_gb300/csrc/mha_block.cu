@@ -35,7 +35,6 @@ namespace {
 constexpr int kBM = 128;       // query rows per CTA
 constexpr int kBN = 64;        // keys per tile (one outer tile)
 constexpr int kThreads = 256;  // warp 0 K loads, warp 1 QK MMAs, warps 2..5 softmax, warp 6 V loads, warp 7 PV MMAs
-constexpr int kMaxCols = 1024; // outer-tile columns supported (Lk <= 65536)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum : int { kEmpty = -1, kFull = -2 };
@@ -54,7 +53,9 @@ struct BlkCfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BM = OFF_V + STAGES * KV_BYTES;  // per stage: part bitmaps of both halves (2 x 512 B)
-  static constexpr int OFF_INFO = OFF_BM + STAGES * 1024;  // then infoA[C], infoB[C], list[C]
+  // column list of this CTA's query tile, laid out like a tile-list slot of the encoded
+  // mask: 16-byte header (count), uint16 col[Cp], int32 kind_a[Cp], int32 kind_b[Cp]
+  static constexpr int OFF_LIST = OFF_BM + STAGES * 1024;
   static constexpr int TMEM_COLS = 256;
   // TMEM columns: S buffers at 0 and 64. With d = 64 there is room for P buffers of their
   // own (columns 128 and 160) and O at 192, so that an S buffer is free again as soon as
@@ -68,10 +69,13 @@ struct BlkCfg {
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(kBM, D, 0, 1);
 };
 
+__host__ __device__ inline int list_cols_padded(int C) { return (C + 7) / 8 * 8; }
+__host__ __device__ inline int list_slot_bytes(int C) { return 16 + 10 * list_cols_padded(C); }
+
 template <int D>
 size_t blk_smem_bytes(int C) {
   using Cfg = BlkCfg<D>;
-  return 1024 + Cfg::OFF_INFO + (size_t)C * 10 + 16;  // OFF_INFO includes the bitmap stages
+  return 1024 + Cfg::OFF_LIST + (size_t)list_slot_bytes(C);
 }
 
 template <int D>
@@ -88,8 +92,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   // buffers) or PV(j) completed (P over S).
   // K stage s is released as soon as its QK has completed (k_empty), V stage s (with the
   // part-tile bitmaps, which the softmax reads) once its PV has completed (v_empty).
-  __shared__ __align__(8) uint64_t q_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST], s_full[2], s_free[2],
-      p_full[2], pv_done[2];
+  __shared__ __align__(8) uint64_t q_full, list_full, k_full[ST], v_full[ST], k_empty[ST], v_empty[ST], s_full[2],
+      s_free[2], p_full[2], pv_done[2];
+  __shared__ int s_ncols;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_rowptr[8];         // full/part row_ptr pairs of outer-tile rows 2qt and 2qt+1
   __shared__ uint32_t s_colbits[32];  // bit c: column c is non-empty in either row (C <= 1024)
@@ -123,14 +128,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   // 1024-byte aligned dynamic shared memory (128-byte swizzle atoms).
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  int32_t* infoA = reinterpret_cast<int32_t*>(smem + Cfg::OFF_INFO);
-  int32_t* infoB = infoA + C;
-  uint16_t* list = reinterpret_cast<uint16_t*>(infoB + C);
+  const int Cp = list_cols_padded(C);
+  uint8_t* lbase = smem + Cfg::OFF_LIST;
+  uint16_t* cols = reinterpret_cast<uint16_t*>(lbase + 16);
+  int32_t* kind_a = reinterpret_cast<int32_t*>(lbase + 16 + 2 * Cp);
+  int32_t* kind_b = kind_a + Cp;
+  const bool have_lists = A.mask.tile_lists != nullptr;
 
-  // ---- setup: barriers, TMEM, union of the two outer-tile rows' columns
-  // The row pointers are fetched first; their latency overlaps the barrier and TMEM setup.
+  // ---- setup: barriers, TMEM, and the column list: the union of the two outer-tile rows'
+  // non-empty columns, copied from the encoded mask's tile lists when present (one bulk
+  // copy), else built here from the CSR arrays. The row pointers / the list copy are
+  // issued first so that their latency overlaps the barrier and TMEM setup.
   int rp = 0;
-  if (threadIdx.x < 8) {
+  if (!have_lists && threadIdx.x < 8) {
     const int a = 2 * qt + (threadIdx.x >> 2);  // threads 0..3: row 2qt, 4..7: row 2qt+1
     if (a < R) {
       const int64_t r = (int64_t)hm * R + a + (threadIdx.x & 1);
@@ -139,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
+    mbar_init(&list_full, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -152,18 +163,29 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&pv_done[s], 1);
     }
     fence_mbar_init();
+    if (have_lists) {
+      const int sb = list_slot_bytes(C);
+      mbar_arrive_expect_tx(&list_full, (uint32_t)sb);
+      bulk_g2s(lbase, A.mask.tile_lists + ((int64_t)hm * ((R + 1) / 2) + qt) * sb, (uint32_t)sb, &list_full);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem_base, Cfg::TMEM_COLS);
     tmem_relinquish();
   }
-  for (int c = threadIdx.x; c < C; c += kThreads) {
-    infoA[c] = kEmpty;
-    infoB[c] = kEmpty;
+  // column-indexed kinds of both rows while the list is built here: scratch in the V stages,
+  // which no load has touched yet
+  int32_t* infoA = reinterpret_cast<int32_t*>(smem + Cfg::OFF_V);
+  int32_t* infoB = infoA + C;
+  if (!have_lists) {
+    for (int c = threadIdx.x; c < C; c += kThreads) {
+      infoA[c] = kEmpty;
+      infoB[c] = kEmpty;
+    }
+    if (threadIdx.x < 8) s_rowptr[threadIdx.x] = rp;
   }
-  if (threadIdx.x < 8) s_rowptr[threadIdx.x] = rp;
   __syncthreads();
-  // Q does not depend on the column union: start its load now, under the union's latency.
+  // Q does not depend on the column list: start its load now, under the list's latency.
   if (threadIdx.x == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -173,26 +195,35 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int kh = 0; kh < Cfg::KH; ++kh)
       tma_load_3d(smem + Cfg::OFF_Q + kh * (kBM * 128), &tm_q, kh * 64, qt * kBM, (int)bh, &q_full);
   }
-  {
-    const int fA0 = s_rowptr[0], fA1 = s_rowptr[1], pA0 = s_rowptr[2], pA1 = s_rowptr[3];
-    const int fB0 = s_rowptr[4], fB1 = s_rowptr[5], pB0 = s_rowptr[6], pB1 = s_rowptr[7];
-    for (int t = fA0 + threadIdx.x; t < fA1; t += kThreads) infoA[A.mask.full_col_idx[t]] = kFull;
-    for (int t = pA0 + threadIdx.x; t < pA1; t += kThreads) infoA[A.mask.part_col_idx[t]] = t;
-    for (int t = fB0 + threadIdx.x; t < fB1; t += kThreads) infoB[A.mask.full_col_idx[t]] = kFull;
-    for (int t = pB0 + threadIdx.x; t < pB1; t += kThreads) infoB[A.mask.part_col_idx[t]] = t;
-  }
-  __syncthreads();
-  // Ascending list of the non-empty columns, built by all warps: one ballot per 32 columns,
-  // a prefix over the (at most 32) words, then every set bit written at its rank.
-  const int nwords = (C + 31) >> 5;
-  int n_cols;  // size of the union (every thread computes it)
-  for (int wd = warp; wd < nwords; wd += kThreads / 32) {
-    const int c = wd * 32 + lane;
-    const unsigned b = __ballot_sync(0xffffffffu, c < C && (infoA[c] != kEmpty || infoB[c] != kEmpty));
-    if (lane == 0) s_colbits[wd] = b;
-  }
-  __syncthreads();
-  {
+  int n_cols;  // size of the union
+  if (have_lists) {
+    if (threadIdx.x == 0) {
+      const int n = mbar_wait(&list_full, 0, A.err, 0x20f) ? *reinterpret_cast<const int*>(lbase) : 0;
+      s_ncols = n < 0 ? 0 : (n > C ? C : n);  // a damaged list cannot index past the buffers
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    n_cols = s_ncols;
+  } else {
+    {
+      const int fA0 = s_rowptr[0], fA1 = s_rowptr[1], pA0 = s_rowptr[2], pA1 = s_rowptr[3];
+      const int fB0 = s_rowptr[4], fB1 = s_rowptr[5], pB0 = s_rowptr[6], pB1 = s_rowptr[7];
+      for (int t = fA0 + threadIdx.x; t < fA1; t += kThreads) infoA[A.mask.full_col_idx[t]] = kFull;
+      for (int t = pA0 + threadIdx.x; t < pA1; t += kThreads) infoA[A.mask.part_col_idx[t]] = t;
+      for (int t = fB0 + threadIdx.x; t < fB1; t += kThreads) infoB[A.mask.full_col_idx[t]] = kFull;
+      for (int t = pB0 + threadIdx.x; t < pB1; t += kThreads) infoB[A.mask.part_col_idx[t]] = t;
+    }
+    __syncthreads();
+    // Ascending list of the non-empty columns, built by all warps: one ballot per 32 columns,
+    // a prefix over the (at most 32) words, then every set bit written at its rank.
+    const int nwords = (C + 31) >> 5;
+    for (int wd = warp; wd < nwords; wd += kThreads / 32) {
+      const int c = wd * 32 + lane;
+      const unsigned b = __ballot_sync(0xffffffffu, c < C && (infoA[c] != kEmpty || infoB[c] != kEmpty));
+      if (lane == 0) s_colbits[wd] = b;
+    }
+    __syncthreads();
     const unsigned wl = lane < nwords ? s_colbits[lane] : 0u;
     int incl = __popc(wl);
 #pragma unroll
@@ -204,17 +235,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int wd = warp; wd < nwords; wd += kThreads / 32) {
       const unsigned b = __shfl_sync(0xffffffffu, wl, wd);
       const int base = __shfl_sync(0xffffffffu, excl, wd);
-      if ((b >> lane) & 1u) list[base + __popc(b & ((1u << lane) - 1u))] = (uint16_t)(wd * 32 + lane);
+      const int c = wd * 32 + lane;
+      if ((b >> lane) & 1u) {
+        const int pos = base + __popc(b & ((1u << lane) - 1u));
+        cols[pos] = (uint16_t)c;
+        kind_a[pos] = infoA[c];
+        kind_b[pos] = infoB[c];
+      }
     }
     n_cols = __shfl_sync(0xffffffffu, incl, 31);
+    tc_fence_before();
+    __syncthreads();  // the list is complete and the scratch in the V stages is dead
+    tc_fence_after();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   // this CTA's chunk of the column list (n_cols <= 1024, n_split <= 1024: no overflow)
   const int jb = chunk * n_cols / n_split;
   const int ntiles = (chunk + 1) * n_cols / n_split - jb;
-  const uint16_t* lst = list + jb;
+  const uint16_t* lst = cols + jb;
+  const int32_t* ka = kind_a + jb;
+  const int32_t* kb = kind_b + jb;
   const uint32_t tmem = s_tmem_base;
   const uint32_t sQ = smem_u32(smem + Cfg::OFF_Q);
   const uint32_t sK = smem_u32(smem + Cfg::OFF_K);
@@ -241,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int s = j % ST;
         if (!mbar_wait(Cfg::PAIR_RING ? &pv_done[s] : &v_empty[s], ((j / ST) & 1u) ^ 1u, A.err, 0x20c)) break;
         const int col = lst[j];
-        const int ia = infoA[col], ib = infoB[col];
+        // (a part index past the mask's part tiles, only possible in a damaged list, fetches nothing)
+        const int ia = ka[j] < A.mask.n_part ? ka[j] : kEmpty, ib = kb[j] < A.mask.n_part ? kb[j] : kEmpty;
         mbar_arrive_expect_tx(&v_full[s], Cfg::KV_BYTES + (ia >= 0 ? 512 : 0) + (ib >= 0 ? 512 : 0));
 #pragma unroll
         for (int kh = 0; kh < Cfg::KH; ++kh)
@@ -303,14 +343,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int qd = warp & 3;             // TMEM lane quadrant of this warp
     const int m = qd * 32 + lane;        // row within the tile
     const int half = m >> 6, r = m & 63;
-    const int32_t* info = half ? infoB : infoA;
+    const int32_t* info = half ? kb : ka;
     const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
     const float c = A.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1, st = j % ST;
-      const int inf = info[lst[j]];  // the same for every row of this warp (one half per warp)
+      const int inf = info[j];  // the same for every row of this warp (one half per warp)
       if (!mbar_wait(&s_full[sb], (j >> 1) & 1, A.err, 0x207)) { ok = false; break; }
       tc_fence_after();
       float s[64];
@@ -539,7 +579,7 @@ sta_status launch_t(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {
 }  // namespace
 
 bool block_kernel_supports(int d, int Lk, int dtype) {
-  return dtype == STA_BF16 && (d == 64 || d == 128) && cdiv(Lk, 64) <= kMaxCols;
+  return dtype == STA_BF16 && (d == 64 || d == 128) && cdiv(Lk, 64) <= kMaxTileListCols;
 }
 
 sta_status launch_mha_block(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {

@@ -171,3 +171,13 @@ def test_mha_splitkv_workspace_query_on_host(lib):
                                    0, 2, None, None, None) == sta.STA_ERR_INVALID_ARG  # no size pointer
     assert lib.sta_mha_fwd_splitkv(16, 16, 16, 16, None, C.byref(m), None, 1, 2, 128, 128, 96, sta.STA_BF16, 0.125,
                                    0, 2, None, C.byref(n), None) == sta.STA_ERR_UNSUPPORTED
+
+
+def test_tile_lists_size_on_host(lib):
+    # ceil(R/2) query tiles per mask head, 16 + 10 * Cp bytes each (Cp = OT columns rounded up to 8)
+    assert lib.sta_tile_lists_bytes(2, 300, 500) == 2 * 3 * (16 + 10 * 8)
+    assert lib.sta_tile_lists_bytes(1, 128, 65536) == 16 + 10 * 1024
+    assert lib.sta_tile_lists_bytes(3, 64, 65) == 3 * (16 + 10 * 8)
+    assert lib.sta_tile_lists_bytes(1, 128, 65537) == 0  # wider than the block kernel
+    assert lib.sta_tile_lists_bytes(0, 128, 128) == 0
+    assert lib.sta_tile_lists_bytes(1, 0, 128) == 0

@@ -10,15 +10,55 @@ from _util import gpu_sources
 pytestmark = pytest.mark.gpu
 
 
+def _expected_tile_lists(ref, Hm, R):
+    """Per (mask head, 128-row query tile): the ascending union of the non-empty OT columns of
+    OT rows 2t and 2t+1 with each row's kind (-1 empty, -2 full, part index), from the
+    oracle's CSR arrays."""
+    out = {}
+    frp, fci, prp, pci = ref["full_row_ptr"], ref["full_col_idx"], ref["part_row_ptr"], ref["part_col_idx"]
+    for hm in range(Hm):
+        for t in range((R + 1) // 2):
+            kinds = []
+            for a in (2 * t, 2 * t + 1):
+                k = {}
+                if a < R:
+                    row = hm * R + a
+                    for i in range(frp[row], frp[row + 1]):
+                        k[int(fci[i])] = -2
+                    for i in range(prp[row], prp[row + 1]):
+                        k[int(pci[i])] = i
+                kinds.append(k)
+            cols = sorted(set(kinds[0]) | set(kinds[1]))
+            out[hm, t] = (cols, [kinds[0].get(c, -1) for c in cols], [kinds[1].get(c, -1) for c in cols])
+    return out
+
+
+def _check_tile_lists(m, ref, Hm, Lq, Lk):
+    R, C = (Lq + 63) // 64, (Lk + 63) // 64
+    Cp = (C + 7) // 8 * 8
+    slot = 16 + 10 * Cp
+    buf = m.tile_lists.cpu().numpy()
+    assert buf.size == Hm * ((R + 1) // 2) * slot
+    for (hm, t), (cols, ka, kb) in _expected_tile_lists(ref, Hm, R).items():
+        b = buf[(hm * ((R + 1) // 2) + t) * slot:][:slot]
+        n = int(b[:4].view(np.int32)[0])
+        assert n == len(cols), (hm, t)
+        np.testing.assert_array_equal(b[16:16 + 2 * Cp].view(np.uint16)[:n], cols)
+        np.testing.assert_array_equal(b[16 + 2 * Cp:16 + 6 * Cp].view(np.int32)[:n], ka)
+        np.testing.assert_array_equal(b[16 + 6 * Cp:16 + 10 * Cp].view(np.int32)[:n], kb)
+
+
 def _check(mask_heads, Lq, Lk, dev):
     import split_kv_decode_bsr_gb300 as sta
 
     ref = oracle.encode_mask(mask_heads, Lq, Lk)
-    got = sta.sta_encode_mask(gpu_sources(mask_heads, dev), Lq, Lk).host_arrays()
+    m = sta.sta_encode_mask(gpu_sources(mask_heads, dev), Lq, Lk)
+    got = m.host_arrays()
     assert (got["n_full"], got["n_part"], got["n_valid"]) == (ref["n_full"], ref["n_part"], ref["n_valid"])
     for key in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx"):
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
     np.testing.assert_array_equal(got["part_bitmap"], ref["part_bitmap"])
+    _check_tile_lists(m, ref, len(mask_heads), Lq, Lk)
     return ref
 
 

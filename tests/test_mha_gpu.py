@@ -19,10 +19,10 @@ def dev(cuda_ok):
     return torch.device("cuda", 0)
 
 
-def _run(wl_q, wl_k, wl_v, mask_heads, head_map, scale, dtype, kernel, dev, Lq, Lk, rows=None):
+def _run(wl_q, wl_k, wl_v, mask_heads, head_map, scale, dtype, kernel, dev, Lq, Lk, rows=None, tile_lists=True):
     import split_kv_decode_bsr_gb300 as sta
 
-    mask = sta.sta_encode_mask(gpu_sources(mask_heads, dev), Lq, Lk)
+    mask = sta.sta_encode_mask(gpu_sources(mask_heads, dev), Lq, Lk, tile_lists=tile_lists)
     q, k, v = to_dev(wl_q, dev), to_dev(wl_k, dev), to_dev(wl_v, dev)
     o, lse = sta.sta_mha_fwd(q, k, v, mask, head_map=head_map, scale=scale, kernel=kernel)
     o = o.float().cpu().numpy()
@@ -58,6 +58,20 @@ def test_random_masks_ragged(dev, kernel, d, Lq, Lk, density):
     u8[0][::5] = 0  # fully masked rows
     heads = [W.MaskHead("u8", data=u8[0]), W.MaskHead("bits", data=W.pack_bits(u8[1]))]
     _run(q, k, v, heads, [1, 0, 1], 1.0 / math.sqrt(d), "bf16", kernel, dev, Lq, Lk)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Lq,Lk,density", [(200, 300, 0.05), (77, 1000, 0.3), (130, 65, 1.0)])
+def test_block_kernel_builds_its_own_column_lists(dev, d, Lq, Lk, density):
+    # mask encoded without tile lists: the block kernel merges the two OT rows itself
+    B, H = 2, 3
+    q = W.make_tensor(6, 1, (B, H, Lq, d), "bf16")
+    k = W.make_tensor(6, 2, (B, H, Lk, d), "bf16")
+    v = W.make_tensor(6, 3, (B, H, Lk, d), "bf16")
+    u8 = [W.random_mask_u8(8, 7, Lq, Lk, density, salt=s) for s in range(2)]
+    u8[0][::5] = 0
+    heads = [W.MaskHead("u8", data=u8[0]), W.MaskHead("bits", data=W.pack_bits(u8[1]))]
+    _run(q, k, v, heads, [1, 0, 1], 1.0 / math.sqrt(d), "bf16", "block", dev, Lq, Lk, tile_lists=False)
 
 
 @pytest.mark.parametrize("kernel", ["block", "row"])
