@@ -2,27 +2,30 @@
 // Q, K, V split into sub-blocks, shared memory plus asynchronous copies overlapping
 // transfer and compute), rebuilt on Blackwell's TMA + tcgen05/TMEM:
 //
-//  * one CTA per (128-row query tile, batch x head). The tile spans outer-tile rows
-//    2t and 2t+1; its key loop runs over the union of their non-empty outer-tile
-//    columns, each half masked by its own class (empty / full / part);
-//  * warp 0 issues TMA loads (128-byte swizzle) of Q once and of K and V tiles of 64
-//    keys into a ring of stages;
-//  * warp 1 owns TMEM (256 columns: two S buffers of 64 columns and the O
-//    accumulator) and issues tcgen05.mma: S = Q K^T (M=128, N=64, K=d, both operands
-//    from shared memory) and O += P V (M=128, N=d, K=64, P read from TMEM),
-//    committing completion to mbarriers;
-//  * warps 2..5 run the softmax, one query row per thread: load the S row from TMEM,
-//    apply the part-tile bitmap (byte r%8 of the 8 inner-tile words of the row, staged
-//    in shared memory by the TMA warp), online max with lazy rescaling (O in TMEM is
-//    rescaled only when the running max grows by more than 2^8, keeping every
-//    exponential below 256), exponentials in base 2 on the MUFU unit, and P rounded
-//    to bf16 and stored back into the first 32 columns of its own S buffer, where the
-//    PV MMA reads it; at the end O / l is written as bf16 and LSE as fp32.
-//  * two CTAs share an SM (256 TMEM columns and < 114 KB of shared memory each), so
-//    one CTA's softmax overlaps the other's MMAs and loads.
-// Empty outer tiles are skipped entirely ("skip, don't reset": 問題定義), full
-// tiles are never masked, iterative tiling over key blocks and one fused loop for
-// max, sum and PV follow Cleave's 複数リダクションのスケジューリング.
+//  * one CTA per (128-row query tile, batch x head[, chunk of the key-tile list]). The tile
+//    spans outer-tile rows 2t and 2t+1; its key loop runs over the union of their non-empty
+//    outer-tile columns (copied from the encoded mask's tile lists, or merged here from the
+//    CSR arrays), each half masked by its own class (empty / full / part);
+//  * warp 0 loads K tiles of 64 keys by TMA (128-byte swizzle) into a ring of stages, warp 6
+//    the V tiles and the part-tile bitmaps; Q is loaded once;
+//  * warp 1 owns TMEM (256 columns: two S buffers of 64 columns, P buffers, the O
+//    accumulator) and issues S = Q K^T (M=128, N=64, K=d, both operands from shared memory);
+//    warp 7 issues O += P V (M=128, N=d, K=64, P read from TMEM). A tcgen05.mma costs its
+//    issuing thread about 60 cycles, so the two products have their own issuing threads;
+//    completion goes to mbarriers through tcgen05.commit;
+//  * warps 2..5 run the softmax, one query row per thread: load the S row from TMEM, apply
+//    the part-tile bitmap (byte r%8 of the 8 inner-tile words of the row, staged in shared
+//    memory), online max with lazy rescaling (O in TMEM is rescaled only when the running
+//    max grows by more than 2^8, keeping every exponential below 256), exponentials in base
+//    2 on the MUFU unit, score scaling and sums on packed fp32 pairs, and P rounded to bf16
+//    into TMEM, where the PV MMA reads it; at the end O / l goes out as bf16 through the idle
+//    Q buffer and a TMA store (or as an fp32 partial when the key list is split), LSE as fp32;
+//  * two CTAs share an SM (256 TMEM columns and < 114 KB of shared memory each), so one
+//    CTA's softmax overlaps the other's MMAs and loads.
+// Empty outer tiles are skipped entirely ("skip, don't reset": 問題定義), full tiles are
+// never masked, iterative tiling over key blocks and one fused loop for max, sum and PV
+// follow Cleave's 複数リダクションのスケジューリング; the split of the key loop with a
+// log-sum-exp merge is Cleave's Split演算子によるSplit-Kの対応.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -124,3 +124,18 @@ def test_longformer_full_size_sampled_rows(dev):
     extra += [31 * L + i for i in range(0, L, 997)]
     rows = _sample_rows(wl.B, wl.H, L, 2000, 2, extra)
     _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "bf16", "block", dev, L, L, rows=rows)
+
+
+def test_mixed_heads_more_tiles_than_resident_ctas(dev):
+    # 384 query tiles of d = 64 (more than two per SM): random part tiles, fully masked rows,
+    # causal and band heads, and a wide score range
+    B, H, L, d = 6, 32, 256, 64
+    q = W.make_tensor(21, 1, (B, H, L, d), "bf16", 2.0)
+    k = W.make_tensor(21, 2, (B, H, L, d), "bf16", 2.0)
+    v = W.make_tensor(21, 3, (B, H, L, d), "bf16")
+    u8 = W.random_mask_u8(22, 7, L, L, 0.4)
+    u8[::9] = 0
+    heads = [W.MaskHead("u8", data=u8), W.pattern(causal=True), W.pattern(win_lo=-40, win_hi=40)]
+    head_map = [h % 3 for h in range(H)]
+    rows = _sample_rows(B, H, L, 4000, 3, extra=[0, L - 1, (B * H - 1) * L + 5])
+    _run(q, k, v, heads, head_map, 0.125, "bf16", "block", dev, L, L, rows=rows)
