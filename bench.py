@@ -36,6 +36,7 @@ import io
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -60,8 +61,14 @@ def load_peaks():
 
 
 def kernel_source_sha(name: str) -> str:
+    """sha1 (12 hex) of a kernel source with comments and whitespace removed: edits to comments
+    keep recorded counters valid, any code change invalidates them."""
     p = os.path.join(ROOT, "split_kv_decode_bsr_gb300", "csrc", name)
-    return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+    src = open(p, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    src = re.sub(r"\s+", " ", src).strip()
+    return hashlib.sha1(src.encode()).hexdigest()[:12]
 
 
 def recorded_traffic(kernel_file: str, workload: str):
