@@ -154,7 +154,9 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
   // -------------------------------------------------------------- consumers
   const int g = g0 + warp;  // kv head of this warp
   const int Hq = A.Hq;
-  float q[G][E], acc[G][E];
+  // q and the output accumulators as packed fp32 pairs (dims 2e, 2e+1 of this lane's E)
+  constexpr int E2 = E / 2;
+  uint64_t q2[G][E2], acc2[G][E2];
   float m_l = -INFINITY, l_l = 0.f;  // running max / sum of head (lane / TG)
   int stage = 0;
   uint32_t round = 0;
@@ -165,16 +167,15 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
     if (inf.flags & kDone) break;
     if (inf.flags & kFirst) {
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(A.q) + ((size_t)inf.r * Hq + (size_t)g * G) * D;
+      const uint64_t sc2 = f32x2_pack(A.scale_log2, A.scale_log2);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qg + h * D + lane * E + e));
-          q[h][e] = bf16lo(w) * A.scale_log2;
-          q[h][e + 1] = bf16hi(w) * A.scale_log2;
+        for (int e = 0; e < E2; ++e) {
+          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qg + h * D + lane * E + 2 * e));
+          q2[h][e] = f32x2_mul(bf16x2_to_f32x2(w), sc2);
+          acc2[h][e] = 0ull;
         }
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
       }
       m_l = -INFINITY;
       l_l = 0.f;
@@ -189,21 +190,23 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
       float vals[32];
 #pragma unroll
       for (int t = 0; t < TG; ++t) {
-        float kf[E];
+        uint64_t k2[E2];
         const __nv_bfloat16* kp = ks + (size_t)(tb + t) * HB * D;
         if constexpr (E == 4) {
           const uint2 w = *reinterpret_cast<const uint2*>(kp);
-          kf[0] = bf16lo(w.x); kf[1] = bf16hi(w.x); kf[2] = bf16lo(w.y); kf[3] = bf16hi(w.y);
+          k2[0] = bf16x2_to_f32x2(w.x);
+          k2[1] = bf16x2_to_f32x2(w.y);
         } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(kp);
-          kf[0] = bf16lo(w); kf[1] = bf16hi(w);
+          k2[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(kp));
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float x = q[h][0] * kf[0];
+          uint64_t x2 = f32x2_mul(q2[h][0], k2[0]);
 #pragma unroll
-          for (int e = 1; e < E; ++e) x = fmaf(q[h][e], kf[e], x);
-          vals[h * TG + t] = x;
+          for (int e = 1; e < E2; ++e) x2 = f32x2_fma(q2[h][e], k2[e], x2);
+          float xl, xh;
+          f32x2_unpack(x2, xl, xh);
+          vals[h * TG + t] = xl + xh;
         }
       }
       // 32-way reduce-scatter: afterwards lane holds the full score of value `lane`.
@@ -236,8 +239,9 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float a_h = s_alpha[warp][h];
+        const uint64_t a2 = f32x2_pack(a_h, a_h);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[h][e] *= a_h;
+        for (int e = 0; e < E2; ++e) acc2[h][e] = f32x2_mul(acc2[h][e], a2);
       }
       const int nv = min(TG, inf.n - tb);
 #pragma unroll 4
@@ -245,19 +249,21 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
         float pv[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) pv[h] = s_p[warp][t * G + h];
-        float vf[E];
+        uint64_t v2[E2];
         const __nv_bfloat16* vp = vs + (size_t)(tb + t) * HB * D;
         if constexpr (E == 4) {
           const uint2 w = *reinterpret_cast<const uint2*>(vp);
-          vf[0] = bf16lo(w.x); vf[1] = bf16hi(w.x); vf[2] = bf16lo(w.y); vf[3] = bf16hi(w.y);
+          v2[0] = bf16x2_to_f32x2(w.x);
+          v2[1] = bf16x2_to_f32x2(w.y);
         } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-          vf[0] = bf16lo(w); vf[1] = bf16hi(w);
+          v2[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(vp));
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
+          const uint64_t p2 = f32x2_pack(pv[h], pv[h]);
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pv[h], vf[e], acc[h][e]);
+          for (int e = 0; e < E2; ++e) acc2[h][e] = f32x2_fma(p2, v2[e], acc2[h][e]);
+        }
       }
       __syncwarp();
     }
@@ -273,16 +279,19 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
         const float inv = l_h > 0.f ? 1.f / l_h : 0.f;
         const float lse_h = l_h > 0.f ? (m_h + log2f(l_h)) * kLn2 : -INFINITY;
         const size_t row = (size_t)g * G + h;
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E2; ++e) f32x2_unpack(acc2[h][e], acc[2 * e], acc[2 * e + 1]);
         if (inf.flags & kFinal) {
           __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + ((size_t)inf.r * Hq + row) * D + lane * E;
 #pragma unroll
           for (int e = 0; e < E; e += 2)
-            *reinterpret_cast<__nv_bfloat162*>(op + e) = __floats2bfloat162_rn(acc[h][e] * inv, acc[h][e + 1] * inv);
+            *reinterpret_cast<__nv_bfloat162*>(op + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
           if (A.lse && lane == 0) A.lse[(size_t)inf.r * Hq + row] = lse_h;
         } else {
           float* op = A.part_o + ((size_t)inf.slot * Hq + row) * D + lane * E;
 #pragma unroll
-          for (int e = 0; e < E; ++e) op[e] = acc[h][e] * inv;
+          for (int e = 0; e < E; ++e) op[e] = acc[e] * inv;
           if (lane == 0) A.part_lse[(size_t)inf.slot * Hq + row] = lse_h;
         }
       }
