@@ -229,7 +229,8 @@ def mha_workload(name):
     import workloads as W
 
     return {"bert-band": W.bert_band, "bigbird": W.bigbird, "longformer": W.longformer,
-            "tiny-causal": W.tiny_causal}[name]()
+            "tiny-causal": W.tiny_causal, "long-causal": W.long_causal,
+            "causal-1head": lambda: W.long_causal(H=1, L=16384)}[name]()
 
 
 def algorithmic_bytes_mha(wl, mask):
@@ -473,8 +474,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
     ap.add_argument("--workload", default="bert-band")
-    ap.add_argument("--extra", default="bigbird,longformer,decode",
-                    help="comma list of secondary workloads (bigbird, longformer, decode) or 'none'")
+    ap.add_argument("--extra", default="bigbird,longformer,decode,long-causal,causal-1head",
+                    help="comma list of secondary workloads (bigbird, longformer, decode, long-causal, "
+                         "causal-1head) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")
@@ -582,6 +584,11 @@ def main():
                                          recorded_traffic(kf, name), peak_src),
                 "gpu_launches": b.launches_per_step() * steps,
             }
+            if b.split:  # the planner cut some heads: time the same call unsplit for comparison
+                nb = MhaBench(name, dev, 1)
+                ms1, _ = time_device(graphed(nb.step), steps, args.warmup, dist, flush)
+                extras[name]["unsplit_ms"] = sum(ms1) / len(ms1)
+                del nb
             if args.sweep_kernels:
                 extras[name]["kernel_ms"] = {
                     k: sum(time_device(graphed(lambda: b.step(k)), steps, args.warmup, dist, flush)[0]) / steps

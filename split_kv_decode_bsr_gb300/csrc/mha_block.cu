@@ -103,7 +103,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ uint32_t s_colbits[32];  // bit c: column c is non-empty in either row (C <= 1024)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
+  // Query tiles in reverse order: the hardware starts blocks x-fastest, and in the common
+  // long-sequence masks (causal, causal windows with global columns) later query tiles
+  // carry more key tiles, so the longest items start first.
+  const int qt = gridDim.x - 1 - blockIdx.x;
   // blockIdx.y enumerates (head rank, batch, chunk): the heaviest heads' tiles are dispatched first
   const int y = blockIdx.y;
   int rank, n_split, off;

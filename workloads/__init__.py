@@ -293,6 +293,15 @@ def bert_band(seed: int = 0, B: int = 8, H: int = 12, L: int = 512, d: int = 64,
                        [pattern(win_lo=-w, win_hi=w)], [0] * H, 1.0 / math.sqrt(d))
 
 
+def long_causal(seed: int = 0, B: int = 1, H: int = 2, L: int = 32768, d: int = 128) -> MhaWorkload:
+    """Few heads over a long causal sequence, bf16: the shape split-KV prefill is for (the
+    last query tiles span 512 key tiles while B*H*L/128 = 512 tiles cannot fill two CTAs
+    per SM evenly)."""
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16", mult=0.5)
+    return MhaWorkload(f"long-causal bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d))
+
+
 def bigbird_blocks(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3):
     """Per mask head and query block: the sorted key-block lists of the BigBird recipe.
 
