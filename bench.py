@@ -230,7 +230,7 @@ def mha_workload(name):
 
     return {"bert-band": W.bert_band, "bigbird": W.bigbird, "longformer": W.longformer,
             "tiny-causal": W.tiny_causal, "long-causal": W.long_causal,
-            "causal-1head": lambda: W.long_causal(H=1, L=16384)}[name]()
+            "causal-1head": lambda: W.long_causal(H=1, L=16384), "sparse-random": W.sparse_random}[name]()
 
 
 def algorithmic_bytes_mha(wl, mask):
@@ -474,9 +474,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
     ap.add_argument("--workload", default="bert-band")
-    ap.add_argument("--extra", default="bigbird,longformer,decode,long-causal,causal-1head",
+    ap.add_argument("--extra", default="bigbird,longformer,decode,long-causal,causal-1head,sparse-random",
                     help="comma list of secondary workloads (bigbird, longformer, decode, long-causal, "
-                         "causal-1head) or 'none'")
+                         "causal-1head, sparse-random) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")

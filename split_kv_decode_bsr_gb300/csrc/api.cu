@@ -36,16 +36,16 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // between the row-wise and the block-wise kernel). Cost model, per query head:
 //   block: every non-empty outer tile costs a 128x64 tile pair of MMAs plus the
 //          softmax of 64x64 scores;   t_b = (n_full + n_part) * 4096 * kBlockPair
-//   row:   every valid (q, k) pair costs 4*d FMA-pipe flops plus a gather;
-//          t_r = n_valid * d * kRowPair
-// The constants come from GB300 measurements (bench.py --sweep-kernels): the
-// block kernel spends about 0.55 ns per computed pair at d = 64 (BigBird) and
-// 0.86 ns at d = 128 (Longformer), the row kernel about 59 ns and 127 ns per
-// valid pair, so the row kernel wins only below ~1% valid density inside the
-// non-empty tiles.
+//   row:   every valid (q, k) pair costs FMA-pipe work, a K and a V row load and a
+//          warp reduction;             t_r = n_valid * d * kRowPair
+// The ratio of the constants comes from GB300 measurements at d = 64 (bench.py
+// --sweep-kernels): on an unstructured mask of 0.4 % density (B=1, H=8, L=4096) the
+// two kernels take 77 us (row) and 82 us (block), i.e. the row kernel spends ~230x
+// the block kernel's time per computed pair on each valid pair, so it wins only below
+// ~0.4 % valid density inside the non-empty tiles; on the BERT band (47 % inside the
+// computed tiles) it takes 312 us against 21 us.
 constexpr double kBlockPairPerD = 1.0 / 64.0;   // relative cost of one computed pair per unit d (block)
-constexpr double kRowPairPerD = 100.0 / 64.0;   // relative cost of one valid pair per unit d (row)
-
+constexpr double kRowPairPerD = 230.0 / 64.0;   // relative cost of one valid pair per unit d (row)
 constexpr int kMaxSplitsPrefill = 1024;
 
 int select_kernel(const sta_bsr_mask* m, int d, int Lk, sta_dtype dtype) {

@@ -1,11 +1,12 @@
 // Row-wise masked MHA kernel (STOF, デュアルカーネル戦略 / 行方向カーネル):
 // Q sliced by rows, one warp per query row, warp shuffles for the softmax
 // reductions and no synchronisation between warps. The warp walks only the
-// non-empty outer tiles of its row (full tiles first, then part tiles, whose
-// 64-bit row mask is gathered from the inner-tile bitmaps), scores up to 32
-// valid keys at a time (one key per lane), and folds them into an fp32 online
-// softmax (running max m, running sum l, output rescaled by exp2(m_old - m_new)).
-// Handles bf16 and fp32 inputs, head dims 64 and 128.
+// non-empty outer tiles of its row: full tiles 32 keys at a time (one key per
+// lane), part tiles through the row's bytes of their inner-tile words, skipping
+// empty inner tiles and scoring each valid key with the head dimensions spread
+// over the lanes. Scores fold into an fp32 online softmax (running max m,
+// running sum l, output rescaled by exp2(m_old - m_new)). Handles bf16 and fp32
+// inputs, head dims 64 and 128.
 #include "internal.h"
 
 namespace sta {
@@ -90,6 +91,11 @@ struct RowIO<D, false> {
 };
 
 // grid (ceil(Lq / 8), B * H), 8 warps: warp w handles query row blockIdx.x * 8 + w.
+// Full tiles are scored 32 keys at a time, one key per lane against q in shared memory.
+// Part tiles are scanned four at a time (lane 8u + w reads inner-tile word w of the row's
+// group in tile u), and each valid key is then scored with the dimensions spread over the
+// lanes (lane owns d/32 of them) and a warp sum, so a sparse row costs work in proportion
+// to its valid keys rather than to the 32 keys of each chunk it touches.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A) {
   using IO = RowIO<D, BF16>;
@@ -103,11 +109,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   const int hm = A.hmap.m[h];
   const int64_t qrow = bh * A.Lq + i;
   const int64_t kv0 = bh * A.Lk;  // first K/V row of this (b, h)
-  {
-    float x[E];
-    IO::load_lane(A.q, qrow, lane, x);
+  float qd[E];                     // this lane's dimensions of q, pre-scaled
+  IO::load_lane(A.q, qrow, lane, qd);
 #pragma unroll
-    for (int e = 0; e < E; ++e) s_q[warp][lane * E + e] = x[e] * A.scale_log2;
+  for (int e = 0; e < E; ++e) {
+    qd[e] *= A.scale_log2;
+    s_q[warp][lane * E + e] = qd[e];
   }
   __syncwarp();
   const float* sq = s_q[warp];
@@ -115,30 +122,21 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   const int64_t mrow = (int64_t)hm * A.mask.ot_rows + a;
   const int fb = A.mask.full_row_ptr[mrow], fe = A.mask.full_row_ptr[mrow + 1];
   const int pb = A.mask.part_row_ptr[mrow], pe = A.mask.part_row_ptr[mrow + 1];
-  const int n_full = fe - fb, n_tiles = n_full + (pe - pb);
 
   float m = -INFINITY, l = 0.f;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
 
-  for (int t = 0; t < n_tiles; ++t) {
-    int col;
-    uint64_t bits;
-    if (t < n_full) {
-      col = A.mask.full_col_idx[fb + t];
-      bits = ~0ull;
-    } else {
-      const int tp = pb + (t - n_full);
-      col = A.mask.part_col_idx[tp];
-      bits = part_row_bits(A.mask.part_bitmap + (int64_t)tp * 64, r);
-    }
+  // ---- full tiles: every key in range is valid
+  for (int t = fb; t < fe; ++t) {
+    const int col = A.mask.full_col_idx[t];
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-      const uint32_t hb = (uint32_t)(bits >> (32 * half));
-      if (hb == 0u) continue;
       const int64_t j0 = (int64_t)col * 64 + half * 32;
-      const bool valid = (hb >> lane) & 1u;
+      if (j0 >= A.Lk) break;
+      const int nk = (int)min((int64_t)32, A.Lk - j0);
+      const bool valid = lane < nk;
       const float s = valid ? IO::dot(sq, A.k, kv0 + j0 + lane) : -INFINITY;
       const float m_new = fmaxf(m, warp_max(s));
       const float alpha = exp2f(m - m_new);  // m = -inf -> 0
@@ -146,9 +144,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
       l = l * alpha + warp_sum(p);
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] *= alpha;
-      if (__popc(hb) >= 8 && j0 + 32 <= A.Lk) {
-        // dense chunk (all 32 keys in range): all 32 V rows, loads independent of the
-        // accumulation (p = 0 for masked keys)
+      if (nk == 32) {
 #pragma unroll 8
         for (int src = 0; src < 32; ++src) {
           const float pj = __shfl_sync(0xffffffffu, p, src);
@@ -158,10 +154,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
           for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, x[e], acc[e]);
         }
       } else {
-        uint32_t vb = hb;
-        while (vb) {
-          const int src = __ffs(vb) - 1;
-          vb &= vb - 1;
+        for (int src = 0; src < nk; ++src) {
           const float pj = __shfl_sync(0xffffffffu, p, src);
           float x[E];
           IO::load_lane(A.v, kv0 + j0 + src, lane, x);
@@ -172,6 +165,59 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
       m = m_new;
     }
   }
+
+  // ---- part tiles: the row's byte of each inner-tile word, four tiles per pass (lane
+  // 8u + w holds word w of tile u); the words of the next pass are requested before the
+  // keys of this one are processed
+  const int wrow = 8 * (r >> 3), sh = (r & 7) * 8;
+  auto scan = [&](int t0, uint32_t& byte, int& col) {
+    const int tt = t0 + (lane >> 3), w = lane & 7;
+    byte = 0u;
+    col = 0;
+    if (tt < pe) {
+      byte = (uint32_t)((__ldg(A.mask.part_bitmap + (int64_t)tt * 64 + wrow + w) >> sh) & 0xFFull);
+      col = __ldg(A.mask.part_col_idx + tt);
+    }
+  };
+  uint32_t byte_next;
+  int col_next;
+  scan(pb, byte_next, col_next);
+  for (int t0 = pb; t0 < pe; t0 += 4) {
+    const uint32_t byte = byte_next;
+    const int col = col_next;
+    if (t0 + 4 < pe) scan(t0 + 4, byte_next, col_next);
+    unsigned nz = __ballot_sync(0xffffffffu, byte != 0u);
+    while (nz) {
+      const int src = __ffs(nz) - 1;
+      nz &= nz - 1;
+      uint32_t bits = __shfl_sync(0xffffffffu, byte, src);
+      const int64_t base = (int64_t)__shfl_sync(0xffffffffu, col, src) * 64 + 8 * (src & 7);
+      while (bits) {
+        const int c = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int64_t j = kv0 + base + c;
+        float kd[E], vd[E];
+        IO::load_lane(A.k, j, lane, kd);
+        IO::load_lane(A.v, j, lane, vd);
+        float part = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) part = fmaf(qd[e], kd[e], part);
+        const float sc = warp_sum(part);
+        if (sc > m) {  // new running max: rescale what has been accumulated (m = -inf -> 0)
+          const float alpha = exp2f(m - sc);
+          l *= alpha;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] *= alpha;
+          m = sc;
+        }
+        const float p = exp2f(sc - m);
+        l += p;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vd[e], acc[e]);
+      }
+    }
+  }
+
   float out[E];
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll

@@ -302,6 +302,17 @@ def long_causal(seed: int = 0, B: int = 1, H: int = 2, L: int = 32768, d: int = 
                        [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d))
 
 
+def sparse_random(seed: int = 0, B: int = 1, H: int = 8, L: int = 4096, d: int = 64,
+                  density: float = 0.004) -> MhaWorkload:
+    """Very sparse unstructured mask (i.i.d. Bernoulli(density), one mask head shared by all
+    heads), bf16: every outer tile is a part tile holding a handful of valid pairs, the case
+    the row-wise kernel is for."""
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16")
+    rnd = MaskHead("bits", data=random_mask_bits(seed, STREAM_MASK_ELEMS, L, L, density))
+    return MhaWorkload(f"sparse-random{density:g} bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       [rnd], [0] * H, 1.0 / math.sqrt(d))
+
+
 def bigbird_blocks(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3):
     """Per mask head and query block: the sorted key-block lists of the BigBird recipe.
 
