@@ -309,7 +309,7 @@ class MhaBench:
 
 
 class DecodeBench:
-    def __init__(self, dev):
+    def __init__(self, dev, page_size: int = 0):
         import torch
 
         import split_kv_decode_bsr_gb300 as sta
@@ -328,11 +328,23 @@ class DecodeBench:
         self.lse = torch.empty((wl.n_req, wl.Hq), dtype=torch.float32, device=dev)
         nbytes = sta.decode_workspace_bytes(self.ind_host, wl.n_req, wl.Hq, wl.Hkv, wl.d, 0)
         self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.page_size = page_size
+        if page_size:  # the same K/V values in pages of page_size tokens, in a random page order
+            pk = W.page_kv(wl, page_size, seed=1)
+            self.kp, self.vp = (host_tensor(t).to(dev) for t in (pk.k_pages, pk.v_pages))
+            self.pind = torch.from_numpy(pk.page_indptr).to(dev)
+            self.pidx = torch.from_numpy(pk.page_indices).to(dev)
+            del self.k, self.v
         self.hq = self.q.cpu().pin_memory()
         self.ho = torch.empty_like(self.o, device="cpu").pin_memory()
         self.hlse = torch.empty_like(self.lse, device="cpu").pin_memory()
 
     def step(self):
+        if self.page_size:
+            self.sta.sta_decode_splitkv_paged(self.q, self.kp, self.vp, self.pind, self.pidx, self.ind, self.ind_host,
+                                              scale=self.wl.scale, num_splits=0, o=self.o, lse=self.lse,
+                                              workspace=self.ws)
+            return
         self.sta.sta_decode_splitkv(self.q, self.k, self.v, self.ind, self.ind_host, scale=self.wl.scale,
                                     num_splits=0, o=self.o, lse=self.lse, workspace=self.ws)
 
@@ -474,8 +486,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
     ap.add_argument("--workload", default="bert-band")
-    ap.add_argument("--extra", default="bigbird,longformer,decode,long-causal,causal-1head,sparse-random",
-                    help="comma list of secondary workloads (bigbird, longformer, decode, long-causal, "
+    ap.add_argument("--extra", default="bigbird,longformer,decode,decode-paged,long-causal,causal-1head,sparse-random",
+                    help="comma list of secondary workloads (bigbird, longformer, decode, decode-paged, long-causal, "
                          "causal-1head, sparse-random) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
@@ -552,15 +564,17 @@ def main():
     wanted = [] if args.extra == "none" else [x for x in args.extra.split(",") if x]
     for name in wanted:
         steps = max(3, min(args.steps, 10))
-        if name == "decode":
-            db = DecodeBench(dev)
+        if name in ("decode", "decode-paged"):
+            db = DecodeBench(dev, 16 if name == "decode-paged" else 0)
             ms, _ = time_device(graphed(db.step), steps, args.warmup, dist, flush)
             t = sum(ms) / len(ms) / 1e3
             gbs = db.kv_bytes / t / 1e9
             e2e_s = time_e2e(db.step_e2e, steps, args.warmup, dist)
-            extras["decode"] = {
+            extras[name] = {
                 "metric": "split-KV decode KV-read GB/s", "value": gbs, "unit": "GB/s", "ms_per_step": 1e3 * t,
-                "config": {"workload": db.wl.name, "T": db.T, "kv_bytes": db.kv_bytes, "num_splits": "auto"},
+                "config": {"workload": db.wl.name, "T": db.T, "kv_bytes": db.kv_bytes, "num_splits": "auto",
+                           "kv_layout": f"paged, {db.page_size} tokens per page, random page order"
+                           if db.page_size else "packed [T, Hkv, d]"},
                 "roofline": roofline_obj("hbm", db.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
                                          recorded_traffic("decode.cu", "decode"), peak_src),
                 "e2e": {"value": db.kv_bytes / (e2e_s / steps) / 1e9, "unit": "GB/s",

@@ -247,6 +247,33 @@ sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const
                               float scale, int num_splits, void* o, float* lse, void* workspace,
                               size_t* workspace_bytes, sta_stream stream);
 
+/* sta_decode_splitkv_paged -- sta_decode_splitkv over a paged KV cache: the
+ * keys and values of all requests live in fixed-size pages, and each request
+ * lists its pages in order (the page-table layout of serving systems; a
+ * deployment variant of the decode, not a step the pages describe).
+ *
+ *   k_pages, v_pages  [n_pages, page_size, Hkv, d] bf16 (device); token i of
+ *                     request r (0-based within the request) is slot
+ *                     i % page_size of page page_indices[page_indptr[r] + i / page_size]
+ *   page_size         tokens per page, >= 1
+ *   n_pages           pages in k_pages / v_pages (page indices are checked against
+ *                     it in the kernel: an index outside [0, n_pages) reads page 0 and
+ *                     sets the device error word to 0x110)
+ *   page_indptr_dev   int32 [n_req+1] (device): request r owns entries
+ *                     page_indptr[r] .. page_indptr[r+1]-1 of page_indices, at least
+ *                     ceil(len_r / page_size) of them
+ *   page_indices_dev  int32 (device) page numbers
+ *   kv_indptr_dev/host token prefix sums [n_req+1] as for sta_decode_splitkv (they give
+ *                     each request's length and the token stream the split divides)
+ * Everything else -- arguments, split plans, workspace, results, errors -- is that
+ * of sta_decode_splitkv; results are identical to it on the same K/V values.
+ * Asynchronous on `stream`. */
+sta_status sta_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages, int page_size,
+                                    int n_pages, const int32_t* page_indptr_dev, const int32_t* page_indices_dev,
+                                    const int32_t* kv_indptr_dev, const int32_t* kv_indptr_host, int n_req, int Hq,
+                                    int Hkv, int d, sta_dtype dtype, float scale, int num_splits, void* o, float* lse,
+                                    void* workspace, size_t* workspace_bytes, sta_stream stream);
+
 /* sta_decode_splitkv_noalloc -- sta_decode_splitkv for callers that cannot
  * allocate device memory: for example code running inside a host framework
  * that owns every device allocation and hands out no allocator, or a serving

@@ -37,7 +37,7 @@ STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
 EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_select_kernel", "sta_decode_splitkv",
-            "sta_decode_splitkv_noalloc", "sta_merge_lse", "sta_status_string", "sta_device_error",
+            "sta_decode_splitkv_noalloc", "sta_decode_splitkv_paged", "sta_merge_lse", "sta_status_string", "sta_device_error",
             "sta_last_cuda_error", "sta_last_cuda_error_string")
 
 BIG = 1 << 40
@@ -86,6 +86,8 @@ def lib():
                                               i32, i32, P, sz, P]
             h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
             h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
+            h.sta_decode_splitkv_paged.argtypes = [P, P, P, i32, i32, P, P, P, P, i32, i32, i32, i32, i32, f32, i32,
+                                                   P, P, P, sz, P]
             h.sta_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P]
             h.sta_merge_lse.argtypes = [P, P, i32, i32, i32, P, i32, P, P]
             h.sta_status_string.argtypes = [i32]
@@ -375,6 +377,37 @@ def sta_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_ind
     _check("sta_decode_splitkv", h.sta_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_indptr_dev), ind, n_req, Hq,
                                                        Hkv, d, _dtype_code(q.dtype), scale, num_splits, _ptr(o),
                                                        _ptr(lse), _ptr(workspace), C.byref(have), _stream(stream)))
+    return o, lse
+
+
+def sta_decode_splitkv_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                             page_indptr_dev: torch.Tensor, page_indices_dev: torch.Tensor, kv_indptr_dev: torch.Tensor,
+                             kv_indptr_host, scale=None, num_splits: int = 0, o=None, lse=None, workspace=None,
+                             stream=None):
+    """GQA decode over a paged KV cache: k_pages/v_pages [n_pages, page_size, Hkv, d] bf16,
+    page_indptr int32 [n_req + 1] and page_indices int32 (device), kv_indptr int32 [n_req + 1]
+    token prefix sums (device and host)."""
+    n_req, Hq, d = q.shape
+    n_pages, page_size, Hkv, dk = k_pages.shape
+    assert dk == d and v_pages.shape == k_pages.shape and kv_indptr_dev.dtype == torch.int32
+    assert page_indptr_dev.dtype == torch.int32 and page_indices_dev.dtype == torch.int32
+    ind = _indptr_host(kv_indptr_host)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((n_req, Hq), dtype=torch.float32, device=q.device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    h = lib()
+    args = lambda ws, nb, st: (_ptr(q), _ptr(k_pages), _ptr(v_pages), page_size, n_pages, _ptr(page_indptr_dev),
+                               _ptr(page_indices_dev), _ptr(kv_indptr_dev), ind, n_req, Hq, Hkv, d,
+                               _dtype_code(q.dtype), scale, num_splits, _ptr(o), _ptr(lse), ws, nb, st)
+    need = C.c_size_t(0)
+    _check("sta_decode_splitkv_paged", h.sta_decode_splitkv_paged(*args(None, C.byref(need), None)))
+    if workspace is None or workspace.numel() < need.value:
+        workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=q.device)
+    have = C.c_size_t(workspace.numel())
+    _check("sta_decode_splitkv_paged",
+           h.sta_decode_splitkv_paged(*args(_ptr(workspace), C.byref(have), _stream(stream))))
     return o, lse
 
 

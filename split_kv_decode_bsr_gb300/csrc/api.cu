@@ -238,10 +238,14 @@ namespace {
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
-extern "C" sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,
-                                         const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d,
-                                         sta_dtype dtype, float scale, int num_splits, void* o, float* lse,
-                                         void* workspace, size_t* workspace_bytes, sta_stream stream) {
+namespace {
+
+// Shared body of the contiguous and the paged decode entry points.
+sta_status decode_call(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,
+                       const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d, sta_dtype dtype, float scale,
+                       int num_splits, void* o, float* lse, void* workspace, size_t* workspace_bytes,
+                       cudaStream_t stream, int page_size, int n_pages, const int32_t* page_indptr,
+                       const int32_t* page_indices) {
   if (!workspace_bytes) return STA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return STA_ERR_INVALID_ARG;
   DecodeArgs a;
@@ -258,6 +262,7 @@ extern "C" sta_status sta_decode_splitkv(const void* q, const void* k, const voi
   if (*workspace_bytes < need) return STA_ERR_WORKSPACE;
   if (!q || !kv_indptr_dev || !o) return STA_ERR_INVALID_ARG;
   if (T > 0 && (!k || !v)) return STA_ERR_INVALID_ARG;  // K/V may be empty (NULL) only when T == 0
+  if (page_size > 0 && T > 0 && (!page_indptr || !page_indices || n_pages < 1)) return STA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)workspace & 255u))
     return STA_ERR_UNSUPPORTED;
   a.q = q; a.k = k; a.v = v; a.kv_indptr = kv_indptr_dev; a.o = o; a.lse = lse;
@@ -265,7 +270,33 @@ extern "C" sta_status sta_decode_splitkv(const void* q, const void* k, const voi
   a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
   a.scale_log2 = scale * kLog2e;
   a.err = device_error_word();
-  return launch_decode(a, (cudaStream_t)stream);
+  a.page_size = page_size;
+  a.n_pages = n_pages;
+  a.page_indptr = page_indptr;
+  a.page_indices = page_indices;
+  return launch_decode(a, stream);
+}
+
+}  // namespace
+
+extern "C" sta_status sta_decode_splitkv(const void* q, const void* k, const void* v, const int32_t* kv_indptr_dev,
+                                         const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d,
+                                         sta_dtype dtype, float scale, int num_splits, void* o, float* lse,
+                                         void* workspace, size_t* workspace_bytes, sta_stream stream) {
+  return decode_call(q, k, v, kv_indptr_dev, kv_indptr_host, n_req, Hq, Hkv, d, dtype, scale, num_splits, o, lse,
+                     workspace, workspace_bytes, (cudaStream_t)stream, 0, 0, nullptr, nullptr);
+}
+
+extern "C" sta_status sta_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages, int page_size,
+                                               int n_pages, const int32_t* page_indptr_dev,
+                                               const int32_t* page_indices_dev, const int32_t* kv_indptr_dev,
+                                               const int32_t* kv_indptr_host, int n_req, int Hq, int Hkv, int d,
+                                               sta_dtype dtype, float scale, int num_splits, void* o, float* lse,
+                                               void* workspace, size_t* workspace_bytes, sta_stream stream) {
+  if (page_size < 1 || n_pages < 0) return STA_ERR_INVALID_ARG;
+  return decode_call(q, k_pages, v_pages, kv_indptr_dev, kv_indptr_host, n_req, Hq, Hkv, d, dtype, scale,
+                     num_splits, o, lse, workspace, workspace_bytes, (cudaStream_t)stream, page_size, n_pages,
+                     page_indptr_dev, page_indices_dev);
 }
 
 extern "C" sta_status sta_merge_lse(const float* part_o, const float* part_lse, int n_rows, int s, int d, void* o,

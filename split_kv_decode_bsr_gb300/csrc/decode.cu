@@ -82,6 +82,41 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
+    // Page cache of the paged layout: lane l holds the page number of ordinal pc_base + l of
+    // request pc_r (warp-uniform bookkeeping; reloaded when a lookup leaves the window).
+    int pc_r = -1, pc_base = 0, pc_page = 0, pc_rb = 0, pc_pb = 0, pc_pe = 0;
+    auto pc_load = [&](int r, int base) {
+      if (r != pc_r) {
+        pc_r = r;
+        pc_rb = __ldg(A.kv_indptr + r);
+        pc_pb = __ldg(A.page_indptr + r);
+        pc_pe = __ldg(A.page_indptr + r + 1);
+      }
+      pc_base = base;
+      const int o = pc_pb + base + lane;
+      pc_page = o < pc_pe ? __ldg(A.page_indices + o) : 0;
+    };
+    auto pc_start = [&](int r) {
+      if (r != pc_r) pc_load(r, 0);
+      return pc_rb;
+    };
+    auto checked = [&](int pg) {
+      if (pg < 0 || pg >= A.n_pages) {  // a bad page table: read page 0, report
+        record_error(A.err, 0x110);
+        pg = 0;
+      }
+      return pg;
+    };
+    // page number of ordinal `ord` (warp-uniform) of request r
+    auto page_of = [&](int r, int ord) {
+      if (r != pc_r || ord < pc_base || ord >= pc_base + 32) pc_load(r, ord);
+      return checked(__shfl_sync(0xffffffffu, pc_page, ord - pc_base));
+    };
+    // per-lane ordinal `mine` within the warp-uniform range [lo, hi] (hi - lo < 32)
+    auto pages_for_stage = [&](int r, int lo, int hi, int mine) {
+      if (r != pc_r || lo < pc_base || hi >= pc_base + 32) pc_load(r, lo);
+      return checked(__shfl_sync(0xffffffffu, pc_page, mine - pc_base));
+    };
     auto emit = [&](int r, int a, int n, int flags, int slot) -> bool {
       if (lane == 0) ok = mbar_wait(&empty_bar[stage], (round & 1u) ^ 1u, A.err, 0x101);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -97,16 +132,43 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
         uint8_t* vs = ks + Cfg::TILE_BYTES;
         const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(A.k);
         const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(A.v);
-        if (HB == Hkv) {
-          if (lane == 0) {
-            const size_t off = (size_t)a * Hkv * D;
-            bulk_g2s(ks, kg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
-            bulk_g2s(vs, vg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
+        if (A.page_size == 0) {
+          if (HB == Hkv) {
+            if (lane == 0) {
+              const size_t off = (size_t)a * Hkv * D;
+              bulk_g2s(ks, kg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
+              bulk_g2s(vs, vg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
+            }
+          } else if (lane < n) {
+            const size_t off = ((size_t)(a + lane) * Hkv + g0) * D;
+            bulk_g2s(ks + lane * HB * D * 2, kg + off, HB * D * 2, &full_bar[stage]);
+            bulk_g2s(vs + lane * HB * D * 2, vg + off, HB * D * 2, &full_bar[stage]);
           }
-        } else if (lane < n) {
-          const size_t off = ((size_t)(a + lane) * Hkv + g0) * D;
-          bulk_g2s(ks + lane * HB * D * 2, kg + off, HB * D * 2, &full_bar[stage]);
-          bulk_g2s(vs + lane * HB * D * 2, vg + off, HB * D * 2, &full_bar[stage]);
+        } else {
+          // paged K/V: tokens a .. a+n-1 of request r, copied page run by page run; the page
+          // numbers come from the warp's page cache (all lanes take part in the lookups)
+          const int P = A.page_size;
+          const int rel0 = a - pc_start(r);  // position of token a within its request
+          if (HB == Hkv) {
+            for (int t = 0; t < n;) {
+              const int rel = rel0 + t;
+              const int run = min(n - t, P - rel % P);
+              const size_t off = ((size_t)page_of(r, rel / P) * P + rel % P) * Hkv * D;
+              if (lane == 0) {
+                bulk_g2s(ks + t * HB * D * 2, kg + off, (uint32_t)(run * HB * D * 2), &full_bar[stage]);
+                bulk_g2s(vs + t * HB * D * 2, vg + off, (uint32_t)(run * HB * D * 2), &full_bar[stage]);
+              }
+              t += run;
+            }
+          } else {
+            const int rel = rel0 + min(lane, n - 1);
+            const int pg = pages_for_stage(r, rel0 / P, (rel0 + n - 1) / P, rel / P);
+            if (lane < n) {
+              const size_t off = (((size_t)pg * P + rel % P) * Hkv + g0) * D;
+              bulk_g2s(ks + lane * HB * D * 2, kg + off, HB * D * 2, &full_bar[stage]);
+              bulk_g2s(vs + lane * HB * D * 2, vg + off, HB * D * 2, &full_bar[stage]);
+            }
+          }
         }
       }
       if (++stage == STAGES) { stage = 0; ++round; }

@@ -69,6 +69,12 @@ struct DecodeArgs {
   int range_len;    // mode 0: tokens per CTA range
   int n_ranges;     // mode 0: number of ranges (CTAs along x)
   int* err;
+  // paged K/V (page_size > 0): k and v are [n_pages, page_size, Hkv, d]; token i of request r
+  // (0-based within the request) is slot i % page_size of page page_indices[page_indptr[r] + i / page_size]
+  int page_size;
+  int n_pages;
+  const int32_t* page_indptr;
+  const int32_t* page_indices;
 };
 
 // Host validation of the decode arguments and the split plan (fills a, T).

@@ -181,3 +181,20 @@ def test_tile_lists_size_on_host(lib):
     assert lib.sta_tile_lists_bytes(1, 128, 65537) == 0  # wider than the block kernel
     assert lib.sta_tile_lists_bytes(0, 128, 128) == 0
     assert lib.sta_tile_lists_bytes(1, 0, 128) == 0
+
+
+def test_paged_decode_rejects_bad_arguments_on_host(lib):
+    ind = (C.c_int32 * 3)(0, 5, 9)
+    n = C.c_size_t(0)
+
+    def call(page_size, n_pages=4, **kw):
+        a = dict(Hq=32, Hkv=8, d=128, splits=0)
+        a.update(kw)
+        return lib.sta_decode_splitkv_paged(None, None, None, page_size, n_pages, None, None, None, ind, 2, a["Hq"],
+                                            a["Hkv"], a["d"], sta.STA_BF16, 0.1, a["splits"], None, None, None,
+                                            C.byref(n), None)
+
+    assert call(0) == sta.STA_ERR_INVALID_ARG
+    assert call(16, n_pages=-1) == sta.STA_ERR_INVALID_ARG
+    assert call(16, Hq=12) == sta.STA_ERR_INVALID_ARG
+    assert call(16, d=96) == sta.STA_ERR_UNSUPPORTED

@@ -435,3 +435,50 @@ def gqa_decode(seed: int = 0, n_req: int = 64, Hq: int = 32, Hkv: int = 8, d: in
     v = make_tensor(seed, STREAM_V, (T, Hkv, d), "bf16")
     return DecodeWorkload(f"gqa-decode bf16 n_req{n_req} Hq{Hq} Hkv{Hkv} d{d} T{T}", n_req, Hq, Hkv, d,
                           "bf16", q, k, v, indptr.astype(np.int32), 1.0 / math.sqrt(d))
+
+
+@dataclass
+class PagedKV:
+    page_size: int
+    k_pages: Tensor        # [n_pages, page_size, Hkv, d]
+    v_pages: Tensor
+    page_indptr: np.ndarray   # int32 [n_req + 1]
+    page_indices: np.ndarray  # int32 [page_indptr[-1]]
+
+
+def page_kv(wl: "DecodeWorkload", page_size: int, seed: int = 0, spare_pages: int = 3,
+            fill: float = 1.0e4) -> PagedKV:
+    """The decode workload's packed K/V laid out in pages of page_size tokens, in a seeded
+    random page order (draws of the mask-block stream), with spare pages and unused slots
+    filled with `fill` so that a read outside a request's tokens shows in the result."""
+    lens = np.diff(wl.kv_indptr.astype(np.int64))
+    n_per = (lens + page_size - 1) // page_size
+    n_used = int(n_per.sum())
+    n_pages = n_used + spare_pages
+    # Fisher-Yates over the page numbers, draws i of the stream
+    perm = np.arange(n_pages, dtype=np.int64)
+    draws = splitmix64(seed, STREAM_MASK_BLOCKS, 1 << 40, max(n_pages, 1))
+    for i in range(n_pages - 1, 0, -1):
+        j = int(draws[i] % np.uint64(i + 1))
+        perm[i], perm[j] = perm[j], perm[i]
+    indptr = np.zeros(len(lens) + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(n_per)
+    indices = perm[:n_used].astype(np.int32)
+    Hkv, d = wl.Hkv, wl.d
+
+    fill_bits = np.uint16(np.array([fill], dtype=np.float32).view(np.uint32)[0] >> 16)  # truncated to bf16
+    fill_f32 = np.array([np.uint32(fill_bits) << np.uint32(16)], dtype=np.uint32).view(np.float32)[0]
+
+    def paged(t: Tensor) -> Tensor:
+        f32 = np.full((n_pages, page_size, Hkv, d), fill_f32, dtype=np.float32)
+        bits = np.full((n_pages, page_size, Hkv, d), fill_bits, dtype=np.uint16)
+        for r, ln in enumerate(lens):
+            rb = int(wl.kv_indptr[r])
+            for pi in range(int(n_per[r])):
+                pg = int(indices[indptr[r] + pi])
+                t0, t1 = pi * page_size, min(int(ln), (pi + 1) * page_size)
+                f32[pg, :t1 - t0] = t.f32[rb + t0:rb + t1]
+                bits[pg, :t1 - t0] = t.bf16[rb + t0:rb + t1]
+        return Tensor(f32, bits)
+
+    return PagedKV(page_size, paged(wl.k), paged(wl.v), indptr.astype(np.int32), indices)
