@@ -265,6 +265,8 @@ class MhaBench:
         self.pairs = valid_pairs(wl, self.head_valid)
         self.flops = 4.0 * wl.d * self.pairs
         self.bytes = algorithmic_bytes_mha(wl, self.mask)
+        # bytes of dense mask input the encoder reads (pattern heads have none)
+        self.encode_input_bytes = sum(int(m.data.nbytes) for m in wl.mask_heads if m.kind in ("bits", "u8"))
         self.kernel = sta.sta_mha_select_kernel(self.mask, wl.B, wl.H, wl.d,
                                                 torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
         self.o = torch.empty_like(self.q)
@@ -598,6 +600,12 @@ def main():
                                          recorded_traffic(kf, name), peak_src),
                 "gpu_launches": b.launches_per_step() * steps,
             }
+            if b.encode_input_bytes:  # the encoder, timed apart: the fill call over the dense mask input
+                ms_e, _ = time_device(graphed(b.mask.refill), steps, args.warmup, dist, flush)
+                te = sum(ms_e) / len(ms_e) / 1e3
+                extras[name]["encode"] = {"us": 1e6 * te, "input_bytes": b.encode_input_bytes,
+                                          "GB/s": b.encode_input_bytes / te / 1e9,
+                                          "frac_hbm": b.encode_input_bytes / te / 1e9 / peaks["hbm_gbs"]}
             if b.split:  # the planner cut some heads: time the same call unsplit for comparison
                 nb = MhaBench(name, dev, 1)
                 ms1, _ = time_device(graphed(nb.step), steps, args.warmup, dist, flush)

@@ -191,6 +191,13 @@ class BsrMask:
         s.tile_lists = self.tile_lists.data_ptr() if self.tile_lists is not None else None
         return s
 
+    def refill(self, stream=None):
+        """Run the encoder's fill call again into this mask's arrays (asynchronous on the stream;
+        the same sources, workspace and capacities as the original encode)."""
+        arr, out, ws, ws_bytes, _ = self._fill
+        _check("sta_encode_mask", lib().sta_encode_mask(arr, self.Hm, self.Lq, self.Lk, C.byref(out), _ptr(ws),
+                                                        C.byref(ws_bytes), _stream(stream)))
+
     def host_arrays(self) -> dict:
         return dict(full_row_ptr=self.full_row_ptr.cpu().numpy(), full_col_idx=self.full_col_idx.cpu().numpy(),
                     part_row_ptr=self.part_row_ptr.cpu().numpy(), part_col_idx=self.part_col_idx.cpu().numpy(),
@@ -248,6 +255,7 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
     m = BsrMask(Hm, Lq, Lk, frp, fci[:nf], prp, pci[:npart], pbm[:npart * 64], nf, npart, nv)
     m.head_tiles = head_tiles
     m.tile_lists = tl
+    m._fill = (arr, out, ws, ws_bytes, srcs)  # keeps the sources alive for refill()
     return m
 
 

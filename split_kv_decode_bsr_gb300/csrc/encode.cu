@@ -2,11 +2,14 @@
 // 64x64 outer tiles classified empty / full / part, full and part tiles listed in
 // two CSR structures, one uint64 bitmap per 8x8 inner tile of each part tile.
 //
-// Three kernels per call: classify (one CTA per (mask head, OT row), warp-level
-// popcounts of the inner-tile words), a single-CTA scan of the per-row counts into
-// row_ptr, and fill (ballot-prefix positions, then the bitmaps of part tiles). When
-// the caller asks for them, a fourth kernel derives the block-wise kernel's column
-// lists (the union of the non-empty columns of each pair of OT rows) from the CSR.
+// Kernels per call: classify (64 outer tiles of one OT row per block; every source is read
+// as 64-bit row words -- bit-packed masks as stored, dense bytes compressed, patterns as
+// intervals -- with popcounts and all-ones tests per tile; the last block to finish scans
+// the per-row counts into row_ptr), fill (column lists by ballot prefixes), and bitmap
+// (one part tile per 64-thread group: its 64 row words transposed into inner-tile words
+// with warp shuffles). When the caller asks for them, a fourth kernel derives the
+// block-wise kernel's column lists (the union of the non-empty columns of each pair of
+// OT rows) from the CSR.
 #include <vector>
 
 #include "common.cuh"
@@ -27,102 +30,92 @@ struct SrcBatch {
   int32_t h0;  // first mask head of this batch
 };
 
-// Bits of row i, columns j0..j0+7 (j0 % 8 == 0): bit c = column j0 + c.
-// Out-of-range rows/columns give 0.
-__device__ __forceinline__ uint32_t row_byte(const SrcDev& s, int Lq, int Lk, int i, int j0) {
-  if (i >= Lq || j0 >= Lk) return 0u;
-  const uint32_t colmask = (Lk - j0 >= 8) ? 0xFFu : ((1u << (Lk - j0)) - 1u);
-  uint32_t b = 0;
-  if (s.kind == STA_MASK_DENSE_BITS) {
-    const int64_t W = (Lk + 63) >> 6;
-    const uint64_t w = static_cast<const uint64_t*>(s.data)[(int64_t)i * W + (j0 >> 6)];
-    b = (uint32_t)((w >> (j0 & 63)) & 0xFFull);
-  } else if (s.kind == STA_MASK_DENSE_U8) {
-    const uint8_t* row = static_cast<const uint8_t*>(s.data) + (int64_t)i * Lk;
-    const int n = min(8, Lk - j0);
-    for (int c = 0; c < n; ++c) b |= (row[j0 + c] != 0 ? 1u : 0u) << c;
-  } else {  // pattern
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int64_t j = j0 + c;
-      const int64_t dd = j - i;
-      bool v = (dd >= s.win_lo && dd <= s.win_hi) || (j < s.n_global);
-      if (s.causal && j > i) v = false;
-      b |= (v ? 1u : 0u) << c;
-    }
-  }
-  return b & colmask;
+// Bits lo..hi (clamped to 0..63) of a 64-bit word; 0 when the range is empty.
+__device__ __forceinline__ uint64_t span_bits(int64_t lo, int64_t hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > 63 ? 63 : hi;
+  if (lo > hi) return 0ull;
+  return (~0ull << lo) & (~0ull >> (63 - hi));
 }
 
-// Inner-tile word (p, q) of outer tile (a, c): bit 8r + cc = element (64a+8p+r, 64c+8q+cc).
-__device__ __forceinline__ uint64_t it_word(const SrcDev& s, int Lq, int Lk, int a, int c, int p, int q) {
-  uint64_t w = 0;
-  const int i0 = a * STA_OT + p * STA_IT, j0 = c * STA_OT + q * STA_IT;
+// 16 mask bytes -> 16 bits (bit k: byte k nonzero). Per 32-bit lane __vsetne4 leaves 0 or 1
+// in each byte; the multiply moves byte k's bit to bit 28 + k with no carries (the other
+// partial products land on distinct bits below 28).
+__device__ __forceinline__ uint32_t u8x16_bits(uint4 v) {
+  const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out = 0;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) w |= (uint64_t)row_byte(s, Lq, Lk, i0 + r, j0) << (8 * r);
+  for (int k = 0; k < 4; ++k) out |= ((__vsetne4(x[k], 0u) * 0x10204080u) >> 28) << (4 * k);
+  return out;
+}
+
+// Row i of the mask over OT column c: bit u = element (i, 64c + u). Rows past Lq give 0,
+// columns past Lk are cleared. Bit-packed masks hold this word as is (one load); dense
+// bytes take four 16-byte loads when rows are 16-byte aligned; patterns are intervals.
+__device__ __forceinline__ uint64_t row_word(const SrcDev& s, int Lq, int Lk, int i, int c) {
+  if (i >= Lq) return 0ull;
+  const int64_t J0 = (int64_t)c * STA_OT;
+  const int valid = Lk - (int)J0;  // columns of this word inside the mask (> 0)
+  uint64_t w;
+  if (s.kind == STA_MASK_DENSE_BITS) {
+    const int64_t W = (Lk + 63) >> 6;
+    w = __ldg(static_cast<const uint64_t*>(s.data) + (int64_t)i * W + c);
+  } else if (s.kind == STA_MASK_DENSE_U8) {
+    const uint8_t* row = static_cast<const uint8_t*>(s.data) + (int64_t)i * Lk + J0;
+    if (valid >= 64 && ((reinterpret_cast<uintptr_t>(row) & 15) == 0)) {
+      const uint4* v = reinterpret_cast<const uint4*>(row);
+      w = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w |= (uint64_t)u8x16_bits(__ldg(v + k)) << (16 * k);
+    } else {
+      w = 0;
+      const int n = valid < 64 ? valid : 64;
+      for (int u = 0; u < n; ++u) w |= (uint64_t)(row[u] != 0) << u;
+    }
+  } else {  // pattern: window [i + win_lo, i + win_hi], global columns [0, n_global), causal j <= i
+    w = span_bits(i + s.win_lo - J0, i + s.win_hi - J0) | span_bits(-J0, s.n_global - 1 - J0);
+    if (s.causal) w &= span_bits(0, i - J0);
+  }
+  if (valid < 64) w &= (1ull << valid) - 1ull;
   return w;
 }
 
-// grid (R, heads in batch), 256 threads: four outer tiles per pass, 64 threads per tile.
-__global__ void __launch_bounds__(256) encode_classify_kernel(SrcBatch batch, int Lq, int Lk, int R, int C,
-                                                              uint8_t* __restrict__ cls, int32_t* __restrict__ full_cnt,
-                                                              int32_t* __restrict__ part_cnt,
-                                                              unsigned long long* __restrict__ valid_cnt) {
-  const SrcDev& src = batch.s[blockIdx.y];
-  const int hm = batch.h0 + blockIdx.y, a = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = tid >> 6, w = tid & 63, p = w >> 3, q = w & 7;
-  __shared__ int s_pop[8], s_all[8];
-  __shared__ int s_nf, s_np;
-  __shared__ unsigned long long s_nv;
-  if (tid == 0) { s_nf = 0; s_np = 0; s_nv = 0; }
-  __syncthreads();
-  const int64_t row = (int64_t)hm * R + a;
-  for (int c0 = 0; c0 < C; c0 += 4) {
-    const int c = c0 + g;
-    const uint64_t word = (c < C) ? it_word(src, Lq, Lk, a, c, p, q) : 0ull;
-    int pop = __popcll(word);
+// The inner-tile word w (= 8p + q) of a 64-thread group whose thread w holds tile row w:
+// word (p, q) is byte q of rows 8p..8p+7, gathered from the 8 lanes of the same warp.
+__device__ __forceinline__ uint64_t transpose_tile_rows(uint64_t row, int w) {
+  const int lane = w & 31, q = w & 7, rbase = lane & ~7;
+  const uint32_t lo = (uint32_t)row, hi = (uint32_t)(row >> 32);
+  uint64_t out = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) pop += __shfl_xor_sync(0xffffffffu, pop, o);
-    const int all = __all_sync(0xffffffffu, word == ~0ull);
-    if (lane == 0) { s_pop[warp] = pop; s_all[warp] = all; }
-    __syncthreads();
-    if (tid < 4 && c0 + tid < C) {
-      const int tot = s_pop[2 * tid] + s_pop[2 * tid + 1];
-      const int full = s_all[2 * tid] && s_all[2 * tid + 1];
-      const uint8_t k = tot == 0 ? 0 : (full ? 1 : 2);
-      cls[row * C + c0 + tid] = k;
-      if (k == 1) atomicAdd(&s_nf, 1);
-      if (k == 2) atomicAdd(&s_np, 1);
-      atomicAdd(&s_nv, (unsigned long long)tot);
-    }
-    __syncthreads();
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t xl = __shfl_sync(0xffffffffu, lo, rbase + r), xh = __shfl_sync(0xffffffffu, hi, rbase + r);
+    const uint32_t byte = q < 4 ? (xl >> (8 * q)) & 0xFFu : (xh >> (8 * (q - 4))) & 0xFFu;
+    out |= (uint64_t)byte << (8 * r);
   }
-  if (tid == 0) {
-    full_cnt[row] = s_nf;
-    part_cnt[row] = s_np;
-    valid_cnt[row] = s_nv;
-  }
+  return out;
 }
 
-// One CTA of 1024 threads: exclusive scans of the per-row counts into row_ptr,
-// totals[0..2] = n_full, n_part, n_valid.
-__global__ void __launch_bounds__(1024) encode_scan_kernel(const int32_t* __restrict__ full_cnt,
-                                                           const int32_t* __restrict__ part_cnt,
-                                                           const unsigned long long* __restrict__ valid_cnt, int n,
-                                                           int32_t* __restrict__ full_row_ptr,
-                                                           int32_t* __restrict__ part_row_ptr,
-                                                           long long* __restrict__ totals) {
-  __shared__ int s_wf[32], s_wp[32];
-  __shared__ unsigned long long s_wv[32];
+constexpr int kClassifyCols = 64;  // outer-tile columns per classify block
+constexpr int kClassifyThreads = 256;
+constexpr int kRowGroups = kClassifyThreads / kClassifyCols;  // threads sharing one outer tile
+constexpr int kRowsPerThread = STA_OT / kRowGroups;
+
+// Exclusive scans of the per-row counts into row_ptr, totals[0..2] = n_full, n_part,
+// n_valid; run by one whole block of kClassifyThreads threads.
+__device__ void scan_row_counts(const int32_t* full_cnt, const int32_t* part_cnt, const unsigned long long* valid_cnt,
+                                int n, int32_t* full_row_ptr, int32_t* part_row_ptr, long long* totals) {
+  constexpr int kWarps = kClassifyThreads / 32;
+  __shared__ int s_wf[kWarps], s_wp[kWarps];
+  __shared__ unsigned long long s_wv[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   long long carry_f = 0, carry_p = 0;
   unsigned long long vsum = 0;
-  for (int base = 0; base < n; base += 1024) {
+  for (int base = 0; base < n; base += kClassifyThreads) {
     const int i = base + tid;
-    const int f = i < n ? full_cnt[i] : 0;
-    const int p = i < n ? part_cnt[i] : 0;
-    unsigned long long v = i < n ? valid_cnt[i] : 0ull;
+    // written by other blocks' atomics: read through L2
+    const int f = i < n ? __ldcg(full_cnt + i) : 0;
+    const int p = i < n ? __ldcg(part_cnt + i) : 0;
+    unsigned long long v = i < n ? __ldcg(valid_cnt + i) : 0ull;
     int xf = f, xp = p;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -136,7 +129,7 @@ __global__ void __launch_bounds__(1024) encode_scan_kernel(const int32_t* __rest
     __syncthreads();
     int off_f = 0, off_p = 0, tot_f = 0, tot_p = 0;
     unsigned long long tot_v = 0;
-    for (int w = 0; w < 32; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
       if (w < warp) { off_f += s_wf[w]; off_p += s_wp[w]; }
       tot_f += s_wf[w];
       tot_p += s_wp[w];
@@ -160,22 +153,99 @@ __global__ void __launch_bounds__(1024) encode_scan_kernel(const int32_t* __rest
   }
 }
 
-// grid (R, heads in batch), 256 threads. Positions come from ballot prefixes over
-// the tile classes in chunks of 256 columns; part-tile bitmaps are recomputed.
-__global__ void __launch_bounds__(256) encode_fill_kernel(SrcBatch batch, int Lq, int Lk, int R, int C,
-                                                          const uint8_t* __restrict__ cls,
+struct ScanOut {
+  unsigned int* done;  // blocks finished, over every classify launch of the call (zeroed before)
+  unsigned int n_blocks;
+  int n_rows;  // Hm * R
+  int32_t* full_row_ptr;
+  int32_t* part_row_ptr;
+  long long* totals;
+};
+
+// grid (R * ceil(C / 64), heads in batch), 256 threads: 64 outer tiles of one OT row per
+// block. Thread (g, u) reads rows g, g + 4, ... of tile column u (for bit-packed masks, 32
+// consecutive words of one row per warp) and keeps the popcount and the all-ones flag; the
+// four row groups are combined in shared memory. The row counts add up across blocks (the
+// counters are zeroed before the first launch) and the last block to finish scans them.
+__global__ void __launch_bounds__(kClassifyThreads) encode_classify_kernel(SrcBatch batch, int Lq, int Lk, int R,
+                                                                          int C, uint8_t* __restrict__ cls,
+                                                                          int32_t* __restrict__ full_cnt,
+                                                                          int32_t* __restrict__ part_cnt,
+                                                                          unsigned long long* __restrict__ valid_cnt,
+                                                                          ScanOut so) {
+  const SrcDev& src = batch.s[blockIdx.y];
+  const int CB = (C + kClassifyCols - 1) / kClassifyCols;
+  const int hm = batch.h0 + blockIdx.y, a = blockIdx.x / CB, cb = blockIdx.x % CB;
+  const int tid = threadIdx.x, lane = tid & 31, g = tid / kClassifyCols, u = tid % kClassifyCols;
+  __shared__ int s_pop[kRowGroups][kClassifyCols];
+  __shared__ int s_all[kRowGroups][kClassifyCols];
+  __shared__ bool s_last;
+  const int c = cb * kClassifyCols + u;
+  const int i0 = a * STA_OT + g;
+  int pop = 0;
+  bool all = true;
+  if (c < C) {
+    if (src.kind == STA_MASK_DENSE_BITS) {  // every load of the thread in flight at once
+      uint64_t rw[kRowsPerThread];
+#pragma unroll
+      for (int k = 0; k < kRowsPerThread; ++k) rw[k] = row_word(src, Lq, Lk, i0 + kRowGroups * k, c);
+#pragma unroll
+      for (int k = 0; k < kRowsPerThread; ++k) {
+        pop += __popcll(rw[k]);
+        all = all && rw[k] == ~0ull;
+      }
+    } else {
+#pragma unroll 4
+      for (int k = 0; k < kRowsPerThread; ++k) {
+        const uint64_t w = row_word(src, Lq, Lk, i0 + kRowGroups * k, c);
+        pop += __popcll(w);
+        all = all && w == ~0ull;
+      }
+    }
+  }
+  s_pop[g][u] = pop;
+  s_all[g][u] = all;
+  __syncthreads();
+  const int64_t row = (int64_t)hm * R + a;
+  if (tid < kClassifyCols) {  // warps 0 and 1: one tile each
+    int tot = 0, full = 1;
+#pragma unroll
+    for (int x = 0; x < kRowGroups; ++x) {
+      tot += s_pop[x][tid];
+      full &= s_all[x][tid];
+    }
+    const int k = c < C ? (tot == 0 ? 0 : (full ? 1 : 2)) : 0;
+    if (c < C) cls[row * C + c] = (uint8_t)k;
+    const int nf = __popc(__ballot_sync(0xffffffffu, k == 1)), np = __popc(__ballot_sync(0xffffffffu, k == 2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane == 0) {
+      if (nf) atomicAdd(&full_cnt[row], nf);
+      if (np) atomicAdd(&part_cnt[row], np);
+      if (tot) atomicAdd(&valid_cnt[row], (unsigned long long)tot);
+      __threadfence();  // the counts are visible before this block counts as done
+    }
+  }
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(so.done, 1u) == so.n_blocks - 1u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  scan_row_counts(full_cnt, part_cnt, valid_cnt, so.n_rows, so.full_row_ptr, so.part_row_ptr, so.totals);
+}
+
+// grid (R, heads in batch), 256 threads: column lists of the full and part tiles, positions
+// from ballot prefixes over the tile classes in chunks of 256 columns.
+__global__ void __launch_bounds__(256) encode_fill_kernel(int hm0, int R, int C, const uint8_t* __restrict__ cls,
                                                           const int32_t* __restrict__ full_row_ptr,
                                                           const int32_t* __restrict__ part_row_ptr,
                                                           int32_t* __restrict__ full_col_idx,
                                                           int32_t* __restrict__ part_col_idx,
                                                           uint64_t* __restrict__ part_bitmap, int64_t cap_full,
                                                           int64_t cap_part) {
-  const SrcDev& src = batch.s[blockIdx.y];
-  const int hm = batch.h0 + blockIdx.y, a = blockIdx.x;
+  const int hm = hm0 + blockIdx.y, a = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = tid >> 6, w = tid & 63, p = w >> 3, q = w & 7;
   __shared__ int s_wf[8], s_wp[8];
-  __shared__ int s_cols[256];
   const int64_t row = (int64_t)hm * R + a;
   const int64_t fbase = full_row_ptr[row], pbase = part_row_ptr[row];
   int64_t run_f = 0, run_p = 0;
@@ -197,18 +267,10 @@ __global__ void __launch_bounds__(256) encode_fill_kernel(SrcBatch batch, int Lq
       if (pos < cap_full) full_col_idx[pos] = c;
     }
     if (k == 2) {
-      const int lp = off_p + __popc(bp & below);
-      s_cols[lp] = c;
-      const int64_t pos = pbase + run_p + lp;
-      if (pos < cap_part) part_col_idx[pos] = c;
-    }
-    __syncthreads();
-    for (int t0 = 0; t0 < tot_p; t0 += 4) {
-      const int t = t0 + g;
-      if (t < tot_p) {
-        const int64_t pos = pbase + run_p + t;
-        const uint64_t word = it_word(src, Lq, Lk, a, s_cols[t], p, q);
-        if (pos < cap_part) part_bitmap[pos * 64 + w] = word;
+      const int64_t pos = pbase + run_p + off_p + __popc(bp & below);
+      if (pos < cap_part) {
+        part_col_idx[pos] = c;
+        part_bitmap[pos * 64] = (uint64_t)row;  // read (then overwritten) by the bitmap kernel
       }
     }
     run_f += tot_f;
@@ -217,10 +279,54 @@ __global__ void __launch_bounds__(256) encode_fill_kernel(SrcBatch batch, int Lq
   }
 }
 
+// Bitmaps of the part tiles: grid ceil(n_part / 4), 256 threads, one part tile per group of
+// 64 threads (one inner-tile word each). The tile's OT row (mask head * R + OT row) is the
+// first word of its bitmap slot, left there by the fill kernel, when one launch covers every
+// mask head (up to 32); with more heads each launch searches part_row_ptr instead, and
+// leaves the tiles of heads outside its batch to their batch.
+__global__ void __launch_bounds__(256) encode_bitmap_kernel(SrcBatch batch, int nb, int Hm, int Lq, int Lk, int R,
+                                                            const int32_t* __restrict__ part_row_ptr,
+                                                            const int32_t* __restrict__ part_col_idx,
+                                                            uint64_t* __restrict__ part_bitmap, int64_t n_part) {
+  const int g = threadIdx.x >> 6, w = threadIdx.x & 63;
+  const int64_t t = (int64_t)blockIdx.x * 4 + g;
+  int hm = -1, a = 0, c = -1;
+  if (t < n_part) {
+    int64_t row;
+    if (nb == Hm) {  // one launch for all heads: the row is in the slot, left there by the fill kernel
+      row = (int64_t)part_bitmap[t * 64];
+    } else {  // several launches: earlier ones have overwritten slots, search part_row_ptr
+      int lo = 0, hi = Hm * R;  // part_row_ptr[lo] <= t < part_row_ptr[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(part_row_ptr + mid) <= t) lo = mid;
+        else hi = mid;
+      }
+      row = lo;
+    }
+    hm = (int)(row / R);
+    a = (int)(row - (int64_t)hm * R);
+    c = __ldg(part_col_idx + t);
+  }
+  __syncthreads();  // every group has read its slot's first word before any group writes
+  const int bh = hm - batch.h0;
+  const bool mine = t < n_part && bh >= 0 && bh < nb;
+  // every thread of the group takes part in the word (warp shuffles); the source is uniform
+  // over the group
+  const SrcDev& src = batch.s[mine ? bh : 0];
+  const uint64_t word = transpose_tile_rows(mine ? row_word(src, Lq, Lk, a * STA_OT + w, c) : 0ull, w);
+  if (mine) part_bitmap[t * 64 + w] = word;
+}
+
+inline int64_t clamp40(int64_t x) {
+  constexpr int64_t kLim = (int64_t)1 << 40;
+  return x < -kLim ? -kLim : (x > kLim ? kLim : x);
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct EncodeWs {
-  size_t cls, full_cnt, part_cnt, valid_cnt, totals, total;
+  size_t cls, full_cnt, part_cnt, valid_cnt, totals, done, total;
 };
 
 EncodeWs encode_ws_layout(int64_t Hm, int64_t R, int64_t C) {
@@ -231,6 +337,7 @@ EncodeWs encode_ws_layout(int64_t Hm, int64_t R, int64_t C) {
   w.part_cnt = off; off += align256(sizeof(int32_t) * Hm * R);
   w.valid_cnt = off; off += align256(sizeof(unsigned long long) * Hm * R);
   w.totals = off; off += align256(sizeof(long long) * 4);
+  w.done = off; off += align256(sizeof(unsigned int));
   w.total = off;
   return w;
 }
@@ -357,22 +464,30 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
       const sta_mask_src& s = srcs[h0 + t];
       b.s[t].kind = s.kind;
       b.s[t].causal = s.causal;
-      b.s[t].win_lo = s.win_lo;
-      b.s[t].win_hi = s.win_hi;
-      b.s[t].n_global = s.n_global_cols;
+      // |j - i| and j stay below 2^30: clamping to +-2^40 keeps every predicate and keeps the
+      // kernels' interval arithmetic clear of int64 overflow
+      b.s[t].win_lo = clamp40(s.win_lo);
+      b.s[t].win_hi = clamp40(s.win_hi);
+      b.s[t].n_global = clamp40(s.n_global_cols);
       b.s[t].data = s.data;
     }
     return b;
   };
+  STA_CUDA_TRY(cudaMemsetAsync(ws + L.full_cnt, 0, L.total - L.full_cnt, st));  // row counters, done count
+  const int64_t CB = cdiv(C, kClassifyCols);
+  ScanOut so;
+  so.done = (unsigned int*)(ws + L.done);
+  so.n_blocks = (unsigned int)(R * CB * Hm);
+  so.n_rows = (int)(Hm * R);
+  so.full_row_ptr = out->full_row_ptr;
+  so.part_row_ptr = out->part_row_ptr;
+  so.totals = totals;
   for (int h0 = 0; h0 < Hm; h0 += kMaxSrcPerLaunch) {
     const int n = Hm - h0 < kMaxSrcPerLaunch ? Hm - h0 : kMaxSrcPerLaunch;
-    encode_classify_kernel<<<dim3((unsigned)R, (unsigned)n), 256, 0, st>>>(make_batch(h0, n), Lq, Lk, (int)R,
-                                                                          (int)C, cls, fcnt, pcnt, vcnt);
+    encode_classify_kernel<<<dim3((unsigned)(R * CB), (unsigned)n), kClassifyThreads, 0, st>>>(
+        make_batch(h0, n), Lq, Lk, (int)R, (int)C, cls, fcnt, pcnt, vcnt, so);
     STA_LAUNCH_CHECK();
   }
-  encode_scan_kernel<<<1, 1024, 0, st>>>(fcnt, pcnt, vcnt, (int)(Hm * R), out->full_row_ptr, out->part_row_ptr,
-                                         totals);
-  STA_LAUNCH_CHECK();
   out->n_mask_heads = Hm;
   out->Lq = Lq;
   out->Lk = Lk;
@@ -401,12 +516,19 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
     }
     return STA_OK;
   }
-  for (int h0 = 0; h0 < Hm; h0 += kMaxSrcPerLaunch) {
-    const int n = Hm - h0 < kMaxSrcPerLaunch ? Hm - h0 : kMaxSrcPerLaunch;
-    encode_fill_kernel<<<dim3((unsigned)R, (unsigned)n), 256, 0, st>>>(
-        make_batch(h0, n), Lq, Lk, (int)R, (int)C, cls, out->full_row_ptr, out->part_row_ptr, out->full_col_idx,
-        out->part_col_idx, out->part_bitmap, out->n_full, out->n_part);
-    STA_LAUNCH_CHECK();
+  encode_fill_kernel<<<dim3((unsigned)R, (unsigned)Hm), 256, 0, st>>>(0, (int)R, (int)C, cls, out->full_row_ptr,
+                                                                      out->part_row_ptr, out->full_col_idx,
+                                                                      out->part_col_idx, out->part_bitmap,
+                                                                      out->n_full, out->n_part);
+  STA_LAUNCH_CHECK();
+  if (out->n_part > 0) {
+    for (int h0 = 0; h0 < Hm; h0 += kMaxSrcPerLaunch) {
+      const int n = Hm - h0 < kMaxSrcPerLaunch ? Hm - h0 : kMaxSrcPerLaunch;
+      encode_bitmap_kernel<<<(unsigned)cdiv(out->n_part, 4), 256, 0, st>>>(
+          make_batch(h0, n), n, Hm, Lq, Lk, (int)R, out->part_row_ptr, out->part_col_idx, out->part_bitmap,
+          out->n_part);
+      STA_LAUNCH_CHECK();
+    }
   }
   if (out->tile_lists) {
     const int Cp = (int)((C + 7) / 8 * 8);

@@ -106,3 +106,37 @@ def test_longformer_structured_and_random_head(dev):
                 W.MaskHead("bits", data=W.random_mask_bits(0, W.STREAM_MASK_ELEMS, L, L, 0.05))]
     ref = _check(wl_heads, L, L, dev)
     assert ref["n_full"] == 762 and ref["n_part"] == 759 + 65536
+
+
+@pytest.mark.parametrize("Lq,Lk", [(70, 128), (129, 257), (256, 1024)])
+def test_pattern_extremes_and_unaligned_bytes(dev, Lq, Lk):
+    # patterns: int64 window edges at their limits, empty windows, global columns past Lk,
+    # a one-diagonal band, an anti-causal window; dense bytes whose rows start off the
+    # 16-byte grid (the source is a view at offset 1..15 of a larger buffer)
+    import torch
+
+    import split_kv_decode_bsr_gb300 as sta
+
+    i64 = np.iinfo(np.int64)
+    pats = [W.pattern(win_lo=int(i64.min), win_hi=int(i64.max)),
+            W.pattern(causal=True, win_lo=int(i64.min), win_hi=-3),
+            W.pattern(win_lo=5, win_hi=4, n_global_cols=2 * Lk),
+            W.pattern(win_lo=5, win_hi=4),
+            W.pattern(causal=True, win_lo=0, win_hi=0, n_global_cols=65),
+            W.pattern(win_lo=1, win_hi=int(i64.max), n_global_cols=int(i64.max)),
+            W.pattern(win_lo=-(Lk + 5), win_hi=-64)]
+    u8 = [W.random_mask_u8(21, 7, Lq, Lk, 0.4, salt=s) for s in range(3)]
+    heads = pats + [W.MaskHead("u8", data=x) for x in u8]
+    ref = oracle.encode_mask(heads, Lq, Lk)
+    srcs = gpu_sources(pats, dev)
+    for off, x in zip((1, 8, 15), u8):
+        buf = torch.zeros(x.size + 16, dtype=torch.uint8, device=dev)
+        view = buf[off:off + x.size]
+        view.copy_(torch.from_numpy(np.ascontiguousarray(x).reshape(-1)))
+        srcs.append(sta.MaskSource.dense_u8(view.view(Lq, Lk)))
+    m = sta.sta_encode_mask(srcs, Lq, Lk)
+    got = m.host_arrays()
+    assert (got["n_full"], got["n_part"], got["n_valid"]) == (ref["n_full"], ref["n_part"], ref["n_valid"])
+    for key in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx", "part_bitmap"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    _check_tile_lists(m, ref, len(heads), Lq, Lk)
