@@ -406,6 +406,14 @@ def time_device(fn, steps, warmup, dist, flush):
     return ms, wall
 
 
+def timing_stats(ms, fn, steps, warmup, dist):
+    """Median and minimum of the cold (L2-flushed) per-step times, and the median with L2
+    left warm (no flush between steps)."""
+    warm, _ = time_device(fn, steps, warmup, dist, lambda: None)
+    return {"cold_median_ms": statistics.median(ms), "cold_min_ms": min(ms),
+            "warm_median_ms": statistics.median(warm), "warm_min_ms": min(warm)}
+
+
 def time_e2e(fn, steps, warmup, dist):
     import torch
 
@@ -521,7 +529,9 @@ def main():
     # ---- headline: masked MHA on the BERT-base band workload
     mb = MhaBench(args.workload, dev, args.mha_splits)
     with ClockSampler(dist.local) as clk:
-        ms, wall = time_device(graphed(mb.step), args.steps, args.warmup, dist, flush)
+        g_mb = graphed(mb.step)
+        ms, wall = time_device(g_mb, args.steps, args.warmup, dist, flush)
+    stats = timing_stats(ms, g_mb, args.steps, args.warmup, dist)
     dev_s = dist.max(sum(ms) / 1e3)
     total_flops = dist.sum(mb.flops * args.steps)
     value = total_flops / dev_s / 1e12
@@ -553,6 +563,7 @@ def main():
         "gpu_launches": mb.launches_per_step() * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
+        "timing_stats": stats,
     }
     line["roofline"]["algorithmic_bytes_per_launch"] = mb.bytes
     if kernel_ms:
@@ -568,7 +579,8 @@ def main():
         steps = max(3, min(args.steps, 10))
         if name in ("decode", "decode-paged"):
             db = DecodeBench(dev, 16 if name == "decode-paged" else 0)
-            ms, _ = time_device(graphed(db.step), steps, args.warmup, dist, flush)
+            g = graphed(db.step)
+            ms, _ = time_device(g, steps, args.warmup, dist, flush)
             t = sum(ms) / len(ms) / 1e3
             gbs = db.kv_bytes / t / 1e9
             e2e_s = time_e2e(db.step_e2e, steps, args.warmup, dist)
@@ -583,11 +595,13 @@ def main():
                         "h2d_bytes_per_step": db.hq.numel() * 2,
                         "d2h_bytes_per_step": db.ho.numel() * 2 + db.hlse.numel() * 4},
                 "gpu_launches": db.launches_per_step() * steps,
+                "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
             }
             del db
         else:
             b = MhaBench(name, dev, args.mha_splits)
-            ms, _ = time_device(graphed(b.step), steps, args.warmup, dist, flush)
+            g = graphed(b.step)
+            ms, _ = time_device(g, steps, args.warmup, dist, flush)
             t = sum(ms) / len(ms) / 1e3
             tf = b.flops / t / 1e12
             kf = "mha_block.cu" if b.kernel == "block" else "mha_row.cu"
@@ -599,11 +613,12 @@ def main():
                 "roofline": roofline_obj("hbm", b.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
                                          recorded_traffic(kf, name), peak_src),
                 "gpu_launches": b.launches_per_step() * steps,
+                "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
             }
             if b.encode_input_bytes:  # the encoder, timed apart: the fill call over the dense mask input
                 ms_e, _ = time_device(graphed(b.mask.refill), steps, args.warmup, dist, flush)
                 te = sum(ms_e) / len(ms_e) / 1e3
-                extras[name]["encode"] = {"us": 1e6 * te, "input_bytes": b.encode_input_bytes,
+                extras[name]["encode"] = {"us": 1e6 * te, "min_us": 1e3 * min(ms_e), "input_bytes": b.encode_input_bytes,
                                           "GB/s": b.encode_input_bytes / te / 1e9,
                                           "frac_hbm": b.encode_input_bytes / te / 1e9 / peaks["hbm_gbs"]}
             if b.split:  # the planner cut some heads: time the same call unsplit for comparison

@@ -5,11 +5,10 @@
 // Kernels per call: classify (64 outer tiles of one OT row per block; every source is read
 // as 64-bit row words -- bit-packed masks as stored, dense bytes compressed, patterns as
 // intervals -- with popcounts and all-ones tests per tile; the last block to finish scans
-// the per-row counts into row_ptr), fill (column lists by ballot prefixes), and bitmap
-// (one part tile per 64-thread group: its 64 row words transposed into inner-tile words
-// with warp shuffles). When the caller asks for them, a fourth kernel derives the
-// block-wise kernel's column lists (the union of the non-empty columns of each pair of
-// OT rows) from the CSR.
+// the per-row counts into row_ptr), fill (column lists by ballot prefixes over a pair of
+// OT rows, and, when the caller asks for them, the block-wise kernel's column lists: the
+// union of the non-empty columns of the pair), and bitmap (one part tile per 64-thread
+// group: its 64 row words transposed into inner-tile words with warp shuffles).
 #include <vector>
 
 #include "common.cuh"
@@ -101,7 +100,10 @@ constexpr int kRowGroups = kClassifyThreads / kClassifyCols;  // threads sharing
 constexpr int kRowsPerThread = STA_OT / kRowGroups;
 
 // Exclusive scans of the per-row counts into row_ptr, totals[0..2] = n_full, n_part,
-// n_valid; run by one whole block of kClassifyThreads threads.
+// n_valid; run by one whole block of kClassifyThreads threads, kScanPerThread consecutive
+// rows per thread and pass (every count of a pass loaded at once).
+constexpr int kScanPerThread = 8;
+
 __device__ void scan_row_counts(const int32_t* full_cnt, const int32_t* part_cnt, const unsigned long long* valid_cnt,
                                 int n, int32_t* full_row_ptr, int32_t* part_row_ptr, long long* totals) {
   constexpr int kWarps = kClassifyThreads / 32;
@@ -110,13 +112,21 @@ __device__ void scan_row_counts(const int32_t* full_cnt, const int32_t* part_cnt
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   long long carry_f = 0, carry_p = 0;
   unsigned long long vsum = 0;
-  for (int base = 0; base < n; base += kClassifyThreads) {
-    const int i = base + tid;
-    // written by other blocks' atomics: read through L2
-    const int f = i < n ? __ldcg(full_cnt + i) : 0;
-    const int p = i < n ? __ldcg(part_cnt + i) : 0;
-    unsigned long long v = i < n ? __ldcg(valid_cnt + i) : 0ull;
-    int xf = f, xp = p;
+  for (int base = 0; base < n; base += kClassifyThreads * kScanPerThread) {
+    const int i0 = base + tid * kScanPerThread;
+    int f[kScanPerThread], p[kScanPerThread];
+    unsigned long long v = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {  // written by other blocks' atomics: read through L2
+      const int i = i0 + e;
+      f[e] = i < n ? __ldcg(full_cnt + i) : 0;
+      p[e] = i < n ? __ldcg(part_cnt + i) : 0;
+      v += i < n ? __ldcg(valid_cnt + i) : 0ull;
+    }
+    int sf = 0, sp = 0;
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) { sf += f[e]; sp += p[e]; }
+    int xf = sf, xp = sp;  // inclusive over the warp's threads
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int yf = __shfl_up_sync(0xffffffffu, xf, o), yp = __shfl_up_sync(0xffffffffu, xp, o);
@@ -135,9 +145,16 @@ __device__ void scan_row_counts(const int32_t* full_cnt, const int32_t* part_cnt
       tot_p += s_wp[w];
       tot_v += s_wv[w];
     }
-    if (i < n) {
-      full_row_ptr[i] = (int32_t)(carry_f + off_f + xf - f);
-      part_row_ptr[i] = (int32_t)(carry_p + off_p + xp - p);
+    long long rf = carry_f + off_f + xf - sf, rp = carry_p + off_p + xp - sp;
+#pragma unroll
+    for (int e = 0; e < kScanPerThread; ++e) {
+      const int i = i0 + e;
+      if (i < n) {
+        full_row_ptr[i] = (int32_t)rf;
+        part_row_ptr[i] = (int32_t)rp;
+      }
+      rf += f[e];
+      rp += p[e];
     }
     carry_f += tot_f;
     carry_p += tot_p;
@@ -234,49 +251,110 @@ __global__ void __launch_bounds__(kClassifyThreads) encode_classify_kernel(SrcBa
   scan_row_counts(full_cnt, part_cnt, valid_cnt, so.n_rows, so.full_row_ptr, so.part_row_ptr, so.totals);
 }
 
-// grid (R, heads in batch), 256 threads: column lists of the full and part tiles, positions
-// from ballot prefixes over the tile classes in chunks of 256 columns.
-__global__ void __launch_bounds__(256) encode_fill_kernel(int hm0, int R, int C, const uint8_t* __restrict__ cls,
+// The block-wise kernel's column list of one (mask head, 128-row query tile) slot from the
+// kinds of the tile's two OT rows (kinds[0..C) row 2t, kinds[C..2C) row 2t+1; -1 empty,
+// -2 full, else the part-tile index): the columns non-empty in either row, ascending, each
+// with both kinds. Slot layout: int32 n (16 bytes), uint16 cols[Cp], int32 ka[Cp], kb[Cp].
+// Run by a whole block (a multiple of 32 threads, C <= 1024).
+__device__ void write_tile_list(const int32_t* kinds, int C, int Cp, uint8_t* slot) {
+  __shared__ uint32_t colbits[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int nwords = (C + 31) >> 5;
+  for (int wd = warp; wd < nwords; wd += nwarps) {
+    const int c = wd * 32 + lane;
+    const unsigned b = __ballot_sync(0xffffffffu, c < C && (kinds[c] != -1 || kinds[C + c] != -1));
+    if (lane == 0) colbits[wd] = b;
+  }
+  __syncthreads();
+  uint16_t* cols = reinterpret_cast<uint16_t*>(slot + 16);
+  int32_t* ka = reinterpret_cast<int32_t*>(slot + 16 + 2 * Cp);
+  int32_t* kb = ka + Cp;
+  const unsigned wl = lane < nwords ? colbits[lane] : 0u;
+  int incl = __popc(wl);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - __popc(wl);
+  for (int wd = warp; wd < nwords; wd += nwarps) {
+    const unsigned b = __shfl_sync(0xffffffffu, wl, wd);
+    const int base = __shfl_sync(0xffffffffu, excl, wd);
+    const int c = wd * 32 + lane;
+    if ((b >> lane) & 1u) {
+      const int pos = base + __popc(b & ((1u << lane) - 1u));
+      cols[pos] = (uint16_t)c;
+      ka[pos] = kinds[c];
+      kb[pos] = kinds[C + c];
+    }
+  }
+  const int n = __shfl_sync(0xffffffffu, incl, 31);
+  if (threadIdx.x == 0) reinterpret_cast<int4*>(slot)[0] = make_int4(n, 0, 0, 0);
+}
+
+// grid (ceil(R / 2), Hm), 256 threads: the column lists of the full and part tiles of OT
+// rows 2t and 2t+1 (positions from ballot prefixes over the tile classes, 256 columns per
+// pass), a marker in the first bitmap word of each part tile (its CSR row, read by the
+// bitmap kernel) and, when lists is set, the block-wise kernel's column-list slot of the
+// pair (dynamic shared memory: int32 kinds[2][C], C <= 1024).
+__global__ void __launch_bounds__(256) encode_fill_kernel(int R, int C, int Cp, const uint8_t* __restrict__ cls,
                                                           const int32_t* __restrict__ full_row_ptr,
                                                           const int32_t* __restrict__ part_row_ptr,
                                                           int32_t* __restrict__ full_col_idx,
                                                           int32_t* __restrict__ part_col_idx,
                                                           uint64_t* __restrict__ part_bitmap, int64_t cap_full,
-                                                          int64_t cap_part) {
-  const int hm = hm0 + blockIdx.y, a = blockIdx.x;
+                                                          int64_t cap_part, uint8_t* __restrict__ lists) {
+  extern __shared__ int32_t kinds[];  // [2][C] when lists != nullptr
+  const int hm = blockIdx.y, t = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ int s_wf[8], s_wp[8];
-  const int64_t row = (int64_t)hm * R + a;
-  const int64_t fbase = full_row_ptr[row], pbase = part_row_ptr[row];
-  int64_t run_f = 0, run_p = 0;
-  for (int c0 = 0; c0 < C; c0 += 256) {
-    const int c = c0 + tid;
-    const int k = c < C ? cls[row * C + c] : 0;
-    const unsigned bf = __ballot_sync(0xffffffffu, k == 1), bp = __ballot_sync(0xffffffffu, k == 2);
-    const unsigned below = (1u << lane) - 1u;
-    if (lane == 0) { s_wf[warp] = __popc(bf); s_wp[warp] = __popc(bp); }
-    __syncthreads();
-    int off_f = 0, off_p = 0, tot_f = 0, tot_p = 0;
-    for (int x = 0; x < 8; ++x) {
-      if (x < warp) { off_f += s_wf[x]; off_p += s_wp[x]; }
-      tot_f += s_wf[x];
-      tot_p += s_wp[x];
+  for (int half = 0; half < 2; ++half) {
+    const int a = 2 * t + half;
+    if (a >= R) {
+      if (lists)
+        for (int c = tid; c < C; c += blockDim.x) kinds[half * C + c] = -1;
+      continue;
     }
-    if (k == 1) {
-      const int64_t pos = fbase + run_f + off_f + __popc(bf & below);
-      if (pos < cap_full) full_col_idx[pos] = c;
-    }
-    if (k == 2) {
-      const int64_t pos = pbase + run_p + off_p + __popc(bp & below);
-      if (pos < cap_part) {
-        part_col_idx[pos] = c;
-        part_bitmap[pos * 64] = (uint64_t)row;  // read (then overwritten) by the bitmap kernel
+    const int64_t row = (int64_t)hm * R + a;
+    const int64_t fbase = full_row_ptr[row], pbase = part_row_ptr[row];
+    int64_t run_f = 0, run_p = 0;
+    for (int c0 = 0; c0 < C; c0 += 256) {
+      const int c = c0 + tid;
+      const int k = c < C ? cls[row * C + c] : 0;
+      const unsigned bf = __ballot_sync(0xffffffffu, k == 1), bp = __ballot_sync(0xffffffffu, k == 2);
+      const unsigned below = (1u << lane) - 1u;
+      if (lane == 0) { s_wf[warp] = __popc(bf); s_wp[warp] = __popc(bp); }
+      __syncthreads();
+      int off_f = 0, off_p = 0, tot_f = 0, tot_p = 0;
+      for (int x = 0; x < 8; ++x) {
+        if (x < warp) { off_f += s_wf[x]; off_p += s_wp[x]; }
+        tot_f += s_wf[x];
+        tot_p += s_wp[x];
       }
+      int32_t kind = -1;
+      if (k == 1) {
+        const int64_t pos = fbase + run_f + off_f + __popc(bf & below);
+        if (pos < cap_full) full_col_idx[pos] = c;
+        kind = -2;
+      }
+      if (k == 2) {
+        const int64_t pos = pbase + run_p + off_p + __popc(bp & below);
+        if (pos < cap_part) {
+          part_col_idx[pos] = c;
+          part_bitmap[pos * 64] = (uint64_t)row;  // read (then overwritten) by the bitmap kernel
+        }
+        kind = (int32_t)pos;
+      }
+      if (lists && c < C) kinds[half * C + c] = kind;
+      run_f += tot_f;
+      run_p += tot_p;
+      __syncthreads();
     }
-    run_f += tot_f;
-    run_p += tot_p;
-    __syncthreads();
   }
+  if (!lists) return;
+  __syncthreads();
+  const int T = (R + 1) / 2;
+  write_tile_list(kinds, C, Cp, lists + ((int64_t)hm * T + t) * (16 + 10 * (int64_t)Cp));
 }
 
 // Bitmaps of the part tiles: grid ceil(n_part / 4), 256 threads, one part tile per group of
@@ -340,64 +418,6 @@ EncodeWs encode_ws_layout(int64_t Hm, int64_t R, int64_t C) {
   w.done = off; off += align256(sizeof(unsigned int));
   w.total = off;
   return w;
-}
-
-// Column lists of the block-wise kernel, one CTA per (query tile t, mask head):
-// the OT columns non-empty in row 2t or 2t+1, ascending, each with the kinds of
-// both rows (-1 empty, -2 full, part-tile index). Dynamic shared memory: two
-// int32 arrays of C (kind of each column per row). C <= 1024.
-__global__ void __launch_bounds__(256) encode_tile_lists_kernel(const int32_t* __restrict__ full_row_ptr,
-                                                                const int32_t* __restrict__ full_col_idx,
-                                                                const int32_t* __restrict__ part_row_ptr,
-                                                                const int32_t* __restrict__ part_col_idx, int R,
-                                                                int C, int Cp, uint8_t* __restrict__ lists) {
-  extern __shared__ int32_t kinds[];  // [2][C]
-  __shared__ uint32_t colbits[32];
-  const int t = blockIdx.x, hm = blockIdx.y, T = (R + 1) / 2;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) kinds[c] = -1;
-  __syncthreads();
-  for (int half = 0; half < 2; ++half) {
-    const int a = 2 * t + half;
-    if (a >= R) continue;
-    const int64_t row = (int64_t)hm * R + a;
-    int32_t* k = kinds + half * C;
-    for (int i = full_row_ptr[row] + threadIdx.x; i < full_row_ptr[row + 1]; i += blockDim.x) k[full_col_idx[i]] = -2;
-    for (int i = part_row_ptr[row] + threadIdx.x; i < part_row_ptr[row + 1]; i += blockDim.x) k[part_col_idx[i]] = i;
-  }
-  __syncthreads();
-  const int nwords = (C + 31) >> 5;
-  for (int wd = warp; wd < nwords; wd += blockDim.x / 32) {
-    const int c = wd * 32 + lane;
-    const unsigned b = __ballot_sync(0xffffffffu, c < C && (kinds[c] != -1 || kinds[C + c] != -1));
-    if (lane == 0) colbits[wd] = b;
-  }
-  __syncthreads();
-  uint8_t* slot = lists + ((int64_t)hm * T + t) * (16 + 10 * (int64_t)Cp);
-  uint16_t* cols = reinterpret_cast<uint16_t*>(slot + 16);
-  int32_t* ka = reinterpret_cast<int32_t*>(slot + 16 + 2 * Cp);
-  int32_t* kb = ka + Cp;
-  const unsigned wl = lane < nwords ? colbits[lane] : 0u;
-  int incl = __popc(wl);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  const int excl = incl - __popc(wl);
-  for (int wd = warp; wd < nwords; wd += blockDim.x / 32) {
-    const unsigned b = __shfl_sync(0xffffffffu, wl, wd);
-    const int base = __shfl_sync(0xffffffffu, excl, wd);
-    const int c = wd * 32 + lane;
-    if ((b >> lane) & 1u) {
-      const int pos = base + __popc(b & ((1u << lane) - 1u));
-      cols[pos] = (uint16_t)c;
-      ka[pos] = kinds[c];
-      kb[pos] = kinds[C + c];
-    }
-  }
-  const int n = __shfl_sync(0xffffffffu, incl, 31);
-  if (threadIdx.x == 0) reinterpret_cast<int4*>(slot)[0] = make_int4(n, 0, 0, 0);
 }
 
 }  // namespace
@@ -516,10 +536,13 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
     }
     return STA_OK;
   }
-  encode_fill_kernel<<<dim3((unsigned)R, (unsigned)Hm), 256, 0, st>>>(0, (int)R, (int)C, cls, out->full_row_ptr,
-                                                                      out->part_row_ptr, out->full_col_idx,
-                                                                      out->part_col_idx, out->part_bitmap,
-                                                                      out->n_full, out->n_part);
+  const int Cp = (int)((C + 7) / 8 * 8);
+  uint8_t* lists = static_cast<uint8_t*>(out->tile_lists);
+  encode_fill_kernel<<<dim3((unsigned)((R + 1) / 2), (unsigned)Hm), 256,
+                       lists ? 2 * C * sizeof(int32_t) : 0, st>>>((int)R, (int)C, Cp, cls, out->full_row_ptr,
+                                                                  out->part_row_ptr, out->full_col_idx,
+                                                                  out->part_col_idx, out->part_bitmap, out->n_full,
+                                                                  out->n_part, lists);
   STA_LAUNCH_CHECK();
   if (out->n_part > 0) {
     for (int h0 = 0; h0 < Hm; h0 += kMaxSrcPerLaunch) {
@@ -529,13 +552,6 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
           out->n_part);
       STA_LAUNCH_CHECK();
     }
-  }
-  if (out->tile_lists) {
-    const int Cp = (int)((C + 7) / 8 * 8);
-    encode_tile_lists_kernel<<<dim3((unsigned)((R + 1) / 2), (unsigned)Hm), 256, 2 * C * sizeof(int32_t), st>>>(
-        out->full_row_ptr, out->full_col_idx, out->part_row_ptr, out->part_col_idx, (int)R, (int)C, Cp,
-        static_cast<uint8_t*>(out->tile_lists));
-    STA_LAUNCH_CHECK();
   }
   return STA_OK;
 }
