@@ -10,8 +10,9 @@ objects, each with its roofline fraction against the measured GB300 peaks.
 A step is one sta_mha_fwd_splitkv call with the library's split plan (the
 block kernel, plus the log-sum-exp merge when a head is split; mask encoded
 once, outside the timed region).
-L2 is flushed (a 256 MiB write, outside the CUDA events) before every timed
-launch. The device time is the sum of per-launch CUDA-event durations on the
+L2 is flushed (a 256 MiB write, then a read of another 256 MiB buffer so that
+no dirty line of the flush is left to write back, outside the CUDA events)
+before every timed launch. The device time is the sum of per-launch CUDA-event durations on the
 launching stream, each around the replay of a CUDA graph holding one library
 call (so that host-side argument handling does not sit between the events);
 `e2e` repeats the step through the public API, without a graph, with the
@@ -361,6 +362,46 @@ class DecodeBench:
         return 2
 
 
+class EpilogueBench:
+    """The fused bias + residual + layer norm after the output projection of a 16384-token,
+    32-head x 128 attention layer: x, residual [16384, 4096] bf16, bias [4096] bf16,
+    gamma, beta [4096] f32 -> y bf16."""
+
+    def __init__(self, dev, rows=16384, n=4096):
+        import torch
+
+        import split_kv_decode_bsr_gb300 as sta
+        import workloads as W
+
+        self.sta, self.rows, self.n = sta, rows, n
+        self.x = host_tensor(W.make_tensor(0, 1, (rows, n), "bf16")).to(dev)
+        self.res = host_tensor(W.make_tensor(0, 2, (rows, n), "bf16", 2.0)).to(dev)
+        self.bias = host_tensor(W.make_tensor(0, 3, (n,), "bf16", 0.5)).to(dev)
+        self.gamma = (1.0 + torch.from_numpy(W.make_tensor(0, 4, (n,), "f32", 0.1).f32)).to(dev)
+        self.beta = torch.from_numpy(W.make_tensor(0, 5, (n,), "f32", 0.1).f32).to(dev)
+        self.y = torch.empty_like(self.x)
+        self.bytes = rows * n * 2 * 3 + n * (2 + 4 + 4)  # x, residual read, y written; the row vectors
+        self.hx = self.x.cpu().pin_memory()
+        self.hy = torch.empty_like(self.y, device="cpu").pin_memory()
+
+    def step(self):
+        self.sta.sta_bias_residual_layernorm(self.x, self.bias, self.res, self.gamma, self.beta, eps=1e-5, y=self.y)
+
+    def step_unfused(self):  # the same operators as three separate torch kernels (context only)
+        import torch
+
+        h = self.x + self.bias + self.res
+        return torch.nn.functional.layer_norm(h, (self.n,), self.gamma.to(h.dtype), self.beta.to(h.dtype), 1e-5)
+
+    def step_e2e(self):
+        self.x.copy_(self.hx, non_blocking=True)
+        self.step()
+        self.hy.copy_(self.y, non_blocking=True)
+
+    def launches_per_step(self):
+        return 1
+
+
 def graphed(fn):
     """One library call captured in a CUDA graph; returns its replay.
 
@@ -496,9 +537,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
     ap.add_argument("--workload", default="bert-band")
-    ap.add_argument("--extra", default="bigbird,longformer,decode,decode-paged,long-causal,causal-1head,sparse-random",
+    ap.add_argument("--extra", default="bigbird,longformer,decode,decode-paged,long-causal,causal-1head,sparse-random,"
+                                       "epilogue-ln,mha-token-major",
                     help="comma list of secondary workloads (bigbird, longformer, decode, decode-paged, long-causal, "
-                         "causal-1head, sparse-random) or 'none'")
+                         "causal-1head, sparse-random, epilogue-ln, mha-token-major) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")
@@ -522,9 +564,14 @@ def main():
     sta.lib()  # fails loudly when libsta.so is missing
     peaks, peak_src = load_peaks()
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean_buf = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
 
     def flush():
+        # a write larger than L2 evicts everything; reading a second such buffer then evicts
+        # the write's own dirty lines, so the timed launch starts from a cold L2 with nothing
+        # of the flush left to write back
         flush_buf.fill_(1)
+        clean_buf.sum()
 
     # ---- headline: masked MHA on the BERT-base band workload
     mb = MhaBench(args.workload, dev, args.mha_splits)
@@ -553,7 +600,7 @@ def main():
         "config": {"workload": mb.wl.name, "B": mb.wl.B, "H": mb.wl.H, "L": mb.wl.Lq, "d": mb.wl.d,
                    "mask": "sliding window |i-j|<=64", "valid_pairs": mb.pairs, "kernel": mb.kernel,
                    "split_kv": "planned" if mb.split else "none",
-                   "l2": "flushed before every timed launch (256 MiB write)", "parallelism": f"replicas x{dist.world}",
+                   "l2": "flushed before every timed launch (256 MiB write, then a 256 MiB read)", "parallelism": f"replicas x{dist.world}",
                    "timing": "CUDA events around a CUDA-graph replay of one library call per step"},
         "tensor_frac": (mb.flops / avg_launch_s / 1e12) / peaks["bf16_tflops"],
         "roofline": roofline_obj("hbm", achieved, peaks["hbm_gbs"], "GB/s", recorded_traffic(kfile, mb.name),
@@ -577,6 +624,54 @@ def main():
     wanted = [] if args.extra == "none" else [x for x in args.extra.split(",") if x]
     for name in wanted:
         steps = max(3, min(args.steps, 10))
+        if name == "epilogue-ln":
+            eb = EpilogueBench(dev)
+            g = graphed(eb.step)
+            ms, _ = time_device(g, steps, args.warmup, dist, flush)
+            t = sum(ms) / len(ms) / 1e3
+            ms_u, _ = time_device(graphed(eb.step_unfused), steps, args.warmup, dist, flush)
+            e2e_s = time_e2e(eb.step_e2e, steps, args.warmup, dist)
+            extras[name] = {
+                "metric": "fused bias+residual+layernorm GB/s", "value": eb.bytes / t / 1e9, "unit": "GB/s",
+                "ms_per_step": 1e3 * t,
+                "config": {"workload": f"bias+residual+layernorm bf16 rows {eb.rows} n {eb.n}",
+                           "algorithmic_bytes": eb.bytes},
+                "roofline": roofline_obj("hbm", eb.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
+                                         recorded_traffic("epilogue.cu", name), peak_src),
+                "unfused_torch_ms": sum(ms_u) / len(ms_u),
+                "e2e": {"value": eb.bytes / (e2e_s / steps) / 1e9, "unit": "GB/s",
+                        "h2d_bytes_per_step": eb.x.numel() * 2, "d2h_bytes_per_step": eb.y.numel() * 2},
+                "gpu_launches": eb.launches_per_step() * steps,
+                "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
+            }
+            del eb
+            continue
+        if name == "mha-token-major":
+            b = MhaBench("longformer", dev, args.mha_splits)
+            ob = torch.empty((b.wl.B, b.wl.Lq, b.wl.H, b.wl.d), dtype=b.q.dtype, device=dev)
+
+            def step_tokens():
+                b.sta.sta_mha_fwd_splitkv(b.q, b.k, b.v, b.mask, head_map=b.wl.head_map, scale=b.wl.scale,
+                                          num_splits=b.num_splits, o=ob, lse=b.lse, workspace=b.ws, o_layout="blhd")
+
+            def step_then_transpose():  # head-major output, then torch's copy into token-major (context only)
+                b.step()
+                ob.copy_(b.o.permute(0, 2, 1, 3))
+
+            ms_t, _ = time_device(graphed(step_tokens), steps, args.warmup, dist, flush)
+            ms_h, _ = time_device(graphed(b.step), steps, args.warmup, dist, flush)
+            ms_x, _ = time_device(graphed(step_then_transpose), steps, args.warmup, dist, flush)
+            t = sum(ms_t) / len(ms_t) / 1e3
+            extras[name] = {
+                "metric": "valid-pair TFLOP/s (masked MHA fwd, O token-major)", "value": b.flops / t / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": 1e3 * t,
+                "config": {"workload": b.wl.name, "o_layout": "[B, L, H, d]", "kernel": b.kernel},
+                "head_major_ms": sum(ms_h) / len(ms_h),
+                "head_major_then_torch_transpose_ms": sum(ms_x) / len(ms_x),
+                "gpu_launches": b.launches_per_step() * steps,
+            }
+            del b, ob
+            continue
         if name in ("decode", "decode-paged"):
             db = DecodeBench(dev, 16 if name == "decode-paged" else 0)
             g = graphed(db.step)

@@ -212,6 +212,48 @@ sta_status sta_mha_fwd_splitkv(const void* q, const void* k, const void* v, void
                                sta_dtype dtype, float scale, int kernel, int num_splits, void* workspace,
                                size_t* workspace_bytes, sta_stream stream);
 
+/* Layouts of O for sta_mha_fwd_layout. */
+#define STA_O_BHLD 0 /* [B, H, Lq, d]: one block of rows per head (as sta_mha_fwd)      */
+#define STA_O_BLHD 1 /* [B, Lq, H, d]: the heads of each query token side by side, i.e. */
+                     /* the [B*Lq, H*d] row-major input of the output projection         */
+
+/* sta_mha_fwd_layout -- sta_mha_fwd_splitkv whose epilogue writes O in the
+ * layout o_layout. STA_O_BLHD merges the heads per token in the same store that
+ * writes O (no separate transpose before the projection GEMM that follows the
+ * attention), the fixed-rule form of fusing MHA with its downstream operators
+ * (STOF, 演算子融合モジュール). Every other argument, the workspace protocol
+ * and the results (element for element, only their places in o differ) are
+ * those of sta_mha_fwd_splitkv; lse stays [B, H, Lq]. o_layout outside the two
+ * values: STA_ERR_INVALID_ARG. */
+sta_status sta_mha_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq, int Lk, int d,
+                              sta_dtype dtype, float scale, int kernel, int num_splits, int o_layout, void* workspace,
+                              size_t* workspace_bytes, sta_stream stream);
+
+/* sta_bias_residual_layernorm -- the elementwise operators that follow the
+ * attention output projection, fused into one pass over each row (STOF,
+ * 演算子融合モジュール, with a fixed fusion rule in place of its search):
+ *   h = (x + bias) + residual
+ *   y = (h - mean(h)) / sqrt(var(h) + eps) * gamma + beta
+ * mean and var over the n elements of the row, var the population variance
+ * (divided by n). Arithmetic in fp32 on the bf16 inputs; y and h_out rounded
+ * to bf16 (round to nearest even).
+ *
+ *   x            [rows, n] bf16 (device), e.g. the projection GEMM's output
+ *   bias         [n] bf16 (device) or NULL (0)
+ *   residual     [rows, n] bf16 (device) or NULL (0)
+ *   gamma, beta  [n] f32 (device) or NULL (1 and 0)
+ *   y            [rows, n] bf16 (device, written; may alias neither input)
+ *   h_out        [rows, n] bf16 (device, written) or NULL: the pre-norm sum h,
+ *                the residual stream of the next sub-layer
+ *   rows >= 0 (0: nothing is launched); n % 8 == 0, 8 <= n <= 16384;
+ *   eps > 0 and finite; dtype STA_BF16 (else STA_ERR_UNSUPPORTED)
+ * Pointers must be 16-byte aligned (else STA_ERR_UNSUPPORTED). One launch,
+ * asynchronous on `stream`. */
+sta_status sta_bias_residual_layernorm(const void* x, const void* bias, const void* residual, const float* gamma,
+                                       const float* beta, void* y, void* h_out, int64_t rows, int n, float eps,
+                                       sta_dtype dtype, sta_stream stream);
+
 /* Which kernel sta_mha_fwd would run for these arguments under
  * STA_KERNEL_AUTO (STA_KERNEL_BLOCK or STA_KERNEL_ROW), or a negative
  * sta_status on invalid arguments. Host only. */

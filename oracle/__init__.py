@@ -17,6 +17,12 @@ it follows:
   (section Split演算子によるSplit-Kの対応; abstract: FlashDecoding) applied to
   the softmax reduction of GQA decode, merged by log-sum-exp.
 
+* ``bias_residual_layernorm`` -- the operators after the attention output
+  projection that STOF's operator-fusion module (section 手法, 演算子融合モジュール)
+  fuses with the MHA layer; the pages name no operator list, so this takes the
+  transformer sub-layer's own: bias add, residual add, layer normalisation
+  (mean and population variance over the row, eps inside the square root).
+
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, invariants, brute force and torch's float64
 ``scaled_dot_product_attention`` (for masks without empty rows). The analytic
@@ -250,3 +256,24 @@ def decode_mask(enc: dict, Hm: int, Lq: int, Lk: int) -> np.ndarray:
     lib.oracle_decode_mask(Hm, Lq, Lk, _ptr(a["full_row_ptr"]), _ptr(a["full_col_idx"]), _ptr(a["part_row_ptr"]),
                            _ptr(a["part_col_idx"]), _ptr(a["part_bitmap"]), _ptr(dense))
     return dense
+
+
+def bias_residual_layernorm(x, bias=None, residual=None, gamma=None, beta=None, eps: float = 1e-5):
+    """Layer normalisation of h = (x + bias) + residual over the last axis, in fp64 on the
+    exact input values: mean = sum(h) / n, var = sum((h - mean)^2) / n,
+    y = (h - mean) / sqrt(var + eps) * gamma + beta. Missing operands are 0 (bias,
+    residual, beta) and 1 (gamma). Returns (y, h) as float64 arrays."""
+    h = np.asarray(x, dtype=np.float64)
+    if bias is not None:
+        h = h + np.asarray(bias, dtype=np.float64)
+    if residual is not None:
+        h = h + np.asarray(residual, dtype=np.float64)
+    n = h.shape[-1]
+    mean = h.sum(axis=-1, keepdims=True) / n
+    var = ((h - mean) ** 2).sum(axis=-1, keepdims=True) / n
+    y = (h - mean) / np.sqrt(var + eps)
+    if gamma is not None:
+        y = y * np.asarray(gamma, dtype=np.float64)
+    if beta is not None:
+        y = y + np.asarray(beta, dtype=np.float64)
+    return y, h

@@ -34,9 +34,11 @@ STA_OK, STA_ERR_INVALID_ARG, STA_ERR_UNSUPPORTED, STA_ERR_WORKSPACE, STA_ERR_CUD
 STA_BF16, STA_F32 = 0, 1
 STA_MASK_PATTERN, STA_MASK_DENSE_U8, STA_MASK_DENSE_BITS = 0, 1, 2
 STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
+STA_O_BHLD, STA_O_BLHD = 0, 1
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
-EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_select_kernel", "sta_decode_splitkv",
+EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_fwd_layout",
+            "sta_bias_residual_layernorm", "sta_mha_select_kernel", "sta_decode_splitkv",
             "sta_decode_splitkv_noalloc", "sta_decode_splitkv_paged", "sta_merge_lse", "sta_status_string", "sta_device_error",
             "sta_last_cuda_error", "sta_last_cuda_error_string")
 
@@ -84,6 +86,9 @@ def lib():
             h.sta_mha_fwd.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32, i32, P]
             h.sta_mha_fwd_splitkv.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32,
                                               i32, i32, P, sz, P]
+            h.sta_mha_fwd_layout.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32,
+                                             i32, i32, i32, P, sz, P]
+            h.sta_bias_residual_layernorm.argtypes = [P, P, P, P, P, P, P, C.c_int64, i32, f32, i32, P]
             h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
             h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
             h.sta_decode_splitkv_paged.argtypes = [P, P, P, i32, i32, P, P, P, P, i32, i32, i32, i32, i32, f32, i32,
@@ -322,27 +327,63 @@ def mha_splitkv_workspace_bytes(mask: BsrMask, B: int, H: int, d: int, dtype=tor
 
 def sta_mha_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BsrMask, head_map=None, scale=None,
                         kernel: str = "auto", num_splits: int = 0, o: Optional[torch.Tensor] = None,
-                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+                        lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None,
+                        o_layout: str = "bhld"):
     """sta_mha_fwd with the block kernel's key-tile loop split into chunks merged by log-sum-exp.
 
     num_splits 0 lets the library choose per head (from mask.head_tiles); s > 0 cuts
     every head's key-tile list into s chunks. workspace: a uint8 device tensor of at
     least mha_splitkv_workspace_bytes(...) bytes (allocated here when None).
+    o_layout "bhld": O is [B, H, Lq, d]; "blhd": O is [B, Lq, H, d] (the heads of each
+    token side by side, written by the same epilogue store; sta_mha_fwd_layout).
     """
+    layout = {"bhld": STA_O_BHLD, "blhd": STA_O_BLHD}[o_layout]
+    if o is None and layout == STA_O_BLHD:
+        B_, H_, Lq_, d_ = q.shape
+        o = torch.empty((B_, Lq_, H_, d_), dtype=q.dtype, device=q.device)
+    if o is not None:
+        assert o.is_contiguous() and o.dtype == q.dtype and o.numel() == q.numel()
     B, H, Lq, Lk, d, o, lse, hm = _mha_common(q, k, v, o, lse, head_map)
     s = mask.struct()
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     h = lib()
     need = C.c_size_t(0)
-    args = (C.byref(s), hm, B, H, Lq, Lk, d, _dtype_code(q.dtype), scale, _KERNELS[kernel], num_splits)
-    _check("sta_mha_fwd_splitkv", h.sta_mha_fwd_splitkv(None, None, None, None, None, *args, None, C.byref(need),
-                                                        None))
+    args = (C.byref(s), hm, B, H, Lq, Lk, d, _dtype_code(q.dtype), scale, _KERNELS[kernel], num_splits, layout)
+    _check("sta_mha_fwd_layout", h.sta_mha_fwd_layout(None, None, None, None, None, *args, None, C.byref(need), None))
     if workspace is None or workspace.numel() < need.value:
         workspace = torch.empty(int(need.value), dtype=torch.uint8, device=q.device)
     have = C.c_size_t(workspace.numel())
-    _check("sta_mha_fwd_splitkv", h.sta_mha_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), *args,
-                                                        _ptr(workspace), C.byref(have), _stream(stream)))
+    _check("sta_mha_fwd_layout", h.sta_mha_fwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), *args,
+                                                      _ptr(workspace), C.byref(have), _stream(stream)))
     return o, lse
+
+
+# ---------------------------------------------------------------------------
+# fused epilogue of the output projection
+
+
+def sta_bias_residual_layernorm(x: torch.Tensor, bias=None, residual=None, gamma=None, beta=None, eps: float = 1e-5,
+                                y: Optional[torch.Tensor] = None, h_out=None, return_sum: bool = False, stream=None):
+    """y = LayerNorm((x + bias) + residual) * gamma + beta over the last dimension, one kernel.
+
+    x, residual [..., n] bf16; bias [n] bf16; gamma, beta [n] float32; any of bias,
+    residual, gamma, beta may be None. return_sum also returns the pre-norm sum
+    (bf16, written by the same kernel into h_out when given).
+    """
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    n = x.shape[-1]
+    rows = x.numel() // n
+    for t, shape, dt in ((bias, (n,), torch.bfloat16), (residual, tuple(x.shape), torch.bfloat16),
+                         (gamma, (n,), torch.float32), (beta, (n,), torch.float32)):
+        if t is not None:
+            assert t.is_contiguous() and tuple(t.shape) == shape and t.dtype == dt and t.device == x.device
+    y = torch.empty_like(x) if y is None else y
+    if return_sum and h_out is None:
+        h_out = torch.empty_like(x)
+    _check("sta_bias_residual_layernorm",
+           lib().sta_bias_residual_layernorm(_ptr(x), _ptr(bias), _ptr(residual), _ptr(gamma), _ptr(beta), _ptr(y),
+                                             _ptr(h_out), rows, n, float(eps), STA_BF16, _stream(stream)))
+    return (y, h_out) if return_sum else y
 
 
 # ---------------------------------------------------------------------------

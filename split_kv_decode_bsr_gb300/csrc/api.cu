@@ -174,15 +174,17 @@ extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, v
   return launch_mha_block(a, plan, s);
 }
 
-extern "C" sta_status sta_mha_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
-                                          const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq,
-                                          int Lk, int d, sta_dtype dtype, float scale, int kernel, int num_splits,
-                                          void* workspace, size_t* workspace_bytes, sta_stream stream) {
+extern "C" sta_status sta_mha_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                         const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq,
+                                         int Lk, int d, sta_dtype dtype, float scale, int kernel, int num_splits,
+                                         int o_layout, void* workspace, size_t* workspace_bytes, sta_stream stream) {
   if (!workspace_bytes || num_splits < 0 || num_splits > kMaxSplitsPrefill) return STA_ERR_INVALID_ARG;
+  if (o_layout != STA_O_BHLD && o_layout != STA_O_BLHD) return STA_ERR_INVALID_ARG;
   MhaArgs a;
   int which = 0;
   sta_status st = mha_prepare(mask, head_map, B, H, Lq, Lk, d, dtype, scale, kernel, a, which);
   if (st != STA_OK) return st;
+  a.o_tokens = o_layout == STA_O_BLHD ? 1 : 0;
   MhaSplit plan;
   size_t need = 256;  // never zero, so that a null workspace always means "query"
   if (which == STA_KERNEL_BLOCK) {
@@ -205,6 +207,14 @@ extern "C" sta_status sta_mha_fwd_splitkv(const void* q, const void* k, const vo
                                              (((rows * (size_t)d * sizeof(float)) + 255) & ~(size_t)255));
   }
   return launch_mha_block(a, plan, s);
+}
+
+extern "C" sta_status sta_mha_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                                          const sta_bsr_mask* mask, const int32_t* head_map, int B, int H, int Lq,
+                                          int Lk, int d, sta_dtype dtype, float scale, int kernel, int num_splits,
+                                          void* workspace, size_t* workspace_bytes, sta_stream stream) {
+  return sta_mha_fwd_layout(q, k, v, o, lse, mask, head_map, B, H, Lq, Lk, d, dtype, scale, kernel, num_splits,
+                            STA_O_BHLD, workspace, workspace_bytes, stream);
 }
 
 namespace sta {

@@ -32,6 +32,7 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+constexpr int kMaxLayerNormCols = 512 * 4 * 8;  // row length of the fused layer norm: 512 threads x 4 vectors of 8
 constexpr int kMaxTileListCols = 1024;  // OT columns the block-wise kernel (and its column lists) support
 
 // Size of the block-wise kernel's per-query-tile column lists (0 if not available).

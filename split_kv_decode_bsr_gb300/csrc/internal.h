@@ -23,7 +23,13 @@ struct MhaArgs {
   int dtype;
   float scale_log2;  // softmax scale * log2(e)
   int* err;          // device error word
+  int o_tokens;      // 0: O is [B, H, Lq, d]; 1: O is [B, Lq, H, d] (heads merged per token)
 };
+
+// Row of d elements of O holding (b, h, query row i), in either layout.
+__host__ __device__ inline int64_t o_row(const MhaArgs& a, int64_t b, int64_t h, int64_t i) {
+  return a.o_tokens ? (b * a.Lq + i) * a.H + h : (b * a.H + h) * a.Lq + i;
+}
 
 // Split-KV plan of the block kernel (Cleave, Split演算子によるSplit-Kの対応 applied to
 // the key-tile loop). grid.y enumerates (launch rank, batch, chunk): rank r covers

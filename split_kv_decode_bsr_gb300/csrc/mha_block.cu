@@ -479,7 +479,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       named_bar_sync(1, 128);
       if (m == 0) {
 #pragma unroll
-        for (int kh = 0; kh < Cfg::KH; ++kh) tma_store_3d(&tm_o, so + kh * (kBM * 128), kh * 64, qt * kBM, (int)bh);
+        for (int kh = 0; kh < Cfg::KH; ++kh) {
+          if (A.o_tokens)  // map (d, H, Lq, B): one head's 128 rows, rows H*d apart
+            tma_store_4d(&tm_o, so + kh * (kBM * 128), kh * 64, (int)(bh % A.H), qt * kBM, (int)(bh / A.H));
+          else
+            tma_store_3d(&tm_o, so + kh * (kBM * 128), kh * 64, qt * kBM, (int)bh);
+        }
         bulk_commit_group();
         bulk_wait_group_read0();  // shared memory is released when the CTA exits
       }
@@ -527,11 +532,11 @@ __global__ void __launch_bounds__(256) mha_split_merge_kernel(const MhaArgs A, c
   const int64_t pr = (int64_t)y0 * A.Lq + row;
   float out[E];
   const float L = merge_row<E>(P.part_o + pr * D, (size_t)A.Lq * D, P.part_lse + pr, (size_t)A.Lq, ns, lane, out);
-  const int64_t orow = ((int64_t)bi * A.H + A.hmap.order[rank]) * A.Lq + row;
-  __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + orow * D + lane * E;
+  const int h = A.hmap.order[rank];
+  __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + o_row(A, bi, h, row) * D + lane * E;
 #pragma unroll
   for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(op + e) = pack_bf16x2(out[e], out[e + 1]);
-  if (A.lse && lane == 0) A.lse[orow] = L;
+  if (A.lse && lane == 0) A.lse[((int64_t)bi * A.H + h) * A.Lq + row] = L;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -559,12 +564,27 @@ bool make_tmap(CUtensorMap* m, const void* base, int d, int L, int BH, int rows)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// O as [B, Lq, H, d] bf16 viewed as a 4-D tensor (d, H, Lq, B); box (64, 1, rows, 1), whose
+// shared-memory image is that of the 3-D box (64, rows, 1) above.
+bool make_tmap_tokens(CUtensorMap* m, const void* base, int d, int H, int L, int B, int rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)L * H * d * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 sta_status launch_t(const MhaArgs& a, const MhaSplit& p, cudaStream_t st) {
   CUtensorMap tq, tk, tv, to;
   const int BH = a.B * a.H;
+  const bool o_ok = a.o_tokens ? make_tmap_tokens(&to, a.o, D, a.H, a.Lq, a.B, kBM) : make_tmap(&to, a.o, D, a.Lq, BH, kBM);
   if (!make_tmap(&tq, a.q, D, a.Lq, BH, kBM) || !make_tmap(&tk, a.k, D, a.Lk, BH, kBN) ||
-      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN) || !make_tmap(&to, a.o, D, a.Lq, BH, kBM)) {
+      !make_tmap(&tv, a.v, D, a.Lk, BH, kBN) || !o_ok) {
     note_cuda_error(cudaErrorInvalidValue);  // tensor-map encoding refused
     return STA_ERR_CUDA;
   }

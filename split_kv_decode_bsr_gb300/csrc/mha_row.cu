@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) out[e] = acc[e] * inv;
-  IO::store_lane(A.o, qrow, lane, out);
+  IO::store_lane(A.o, o_row(A, bh / A.H, h, i), lane, out);
   if (A.lse && lane == 0) A.lse[qrow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 

@@ -405,3 +405,65 @@ def test_encode_decode_round_trip_and_tile_rules(Lq, Lk, density):
         for a in range(len(rp) - 1):
             assert (np.diff(ci[rp[a]:rp[a + 1]]) > 0).all()
     assert all(enc["part_bitmap"][t].any() for t in range(enc["n_part"]))
+
+
+# ---- bias + residual + layer norm (the fused epilogue after the output projection)
+
+
+@pytest.mark.parametrize("n", [8, 24, 768])
+def test_layernorm_matches_torch_fp64(n):
+    # the library routine on h = (x + bias) + residual; row 0 has a spread far below
+    # sqrt(eps), where eps decides the scale
+    rng = np.random.default_rng(n)
+    rows = 6
+    x = rng.normal(size=(rows, n))
+    b = rng.normal(size=n)
+    r = rng.normal(size=(rows, n)) * 3.0
+    x[0] = -b + rng.normal(size=n) * 1e-4
+    r[0] = 0.0
+    g = rng.normal(1.0, 0.2, size=n)
+    be = rng.normal(0.0, 0.2, size=n)
+    for eps in (1e-5, 1e-12):
+        y, h = oracle.bias_residual_layernorm(x, b, r, g, be, eps=eps)
+        ref = torch.nn.functional.layer_norm(torch.from_numpy(x + b + r), (n,), torch.from_numpy(g),
+                                             torch.from_numpy(be), eps=eps)
+        assert np.abs(y - ref.numpy()).max() < 1e-10
+        assert np.array_equal(h, (x + b) + r)
+
+
+def test_layernorm_two_element_rows_closed_form():
+    # (a, c): mean (a + c) / 2, var = delta^2 with delta = (a - c) / 2, so
+    # y = (+-delta) / sqrt(delta^2 + eps)
+    for a, c, eps in ((3.0, 1.0, 1e-5), (0.5, 0.5, 1e-3), (-2.0, 6.0, 0.25), (1e-3, -1e-3, 1e-6)):
+        y, _ = oracle.bias_residual_layernorm(np.array([[a, c]]), eps=eps)
+        dl = (a - c) / 2.0
+        want = np.array([dl, -dl]) / math.sqrt(dl * dl + eps)
+        assert np.abs(y[0] - want).max() < 1e-15
+
+
+def test_layernorm_constant_rows_give_beta():
+    be = np.linspace(-1.0, 1.0, 16)
+    g = np.linspace(0.5, 2.0, 16)
+    y, _ = oracle.bias_residual_layernorm(np.full((3, 16), 7.25), None, np.full((3, 16), -0.5), g, be, eps=1e-5)
+    assert np.array_equal(y, np.broadcast_to(be, (3, 16)))
+
+
+def test_layernorm_shift_and_scale_invariance():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(4, 64))
+    y0, _ = oracle.bias_residual_layernorm(x, eps=1e-5)
+    y1, _ = oracle.bias_residual_layernorm(x, None, np.full((4, 64), 5.0), eps=1e-5)  # a constant residual
+    y2, _ = oracle.bias_residual_layernorm(8.0 * x, eps=64.0 * 1e-5)  # x * s with eps * s^2
+    assert np.abs(y1 - y0).max() < 1e-12
+    assert np.abs(y2 - y0).max() < 1e-12
+
+
+def test_layernorm_normalised_moments():
+    # gamma 1, beta 0: every row has mean 0 and mean square var / (var + eps)
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(5, 40)) * np.array([[0.01], [0.1], [1.0], [3.0], [100.0]])
+    eps = 1e-4
+    y, h = oracle.bias_residual_layernorm(x, eps=eps)
+    var = h.var(axis=-1)
+    assert np.abs(y.mean(axis=-1)).max() < 1e-12
+    assert np.abs((y ** 2).mean(axis=-1) - var / (var + eps)).max() < 1e-12
