@@ -564,7 +564,7 @@ def main():
     sta.lib()  # fails loudly when libsta.so is missing
     peaks, peak_src = load_peaks()
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    clean_buf = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+    clean_buf = torch.zeros(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB, summed in place
 
     def flush():
         # a write larger than L2 evicts everything; reading a second such buffer then evicts
