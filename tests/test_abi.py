@@ -198,3 +198,41 @@ def test_paged_decode_rejects_bad_arguments_on_host(lib):
     assert call(16, n_pages=-1) == sta.STA_ERR_INVALID_ARG
     assert call(16, Hq=12) == sta.STA_ERR_INVALID_ARG
     assert call(16, d=96) == sta.STA_ERR_UNSUPPORTED
+
+
+def test_mha_layout_rejects_bad_layouts_on_host(lib):
+    m = _mask_struct()
+    n = C.c_size_t(0)
+
+    def call(layout):
+        return lib.sta_mha_fwd_layout(None, None, None, None, None, C.byref(m), None, 1, 2, 128, 128, 64, sta.STA_BF16,
+                                      0.125, 0, 2, layout, None, C.byref(n), None)
+
+    assert call(sta.STA_O_BHLD) == sta.STA_OK and n.value >= 256  # the size query, as for sta_mha_fwd_splitkv
+    assert call(sta.STA_O_BLHD) == sta.STA_OK
+    assert call(2) == sta.STA_ERR_INVALID_ARG
+    assert call(-1) == sta.STA_ERR_INVALID_ARG
+
+
+def test_layernorm_rejects_bad_arguments_on_host(lib):
+    # every check runs on the host before any launch; rows == 0 launches nothing
+    p = C.c_void_p(1 << 20)  # aligned dummy device pointers (never dereferenced here)
+
+    def call(x=p, rows=4, n=64, eps=1e-5, dtype=sta.STA_BF16, y=p, bias=None, gamma=None):
+        return lib.sta_bias_residual_layernorm(x, bias, None, gamma, None, y, None, rows, n, eps, dtype, None)
+
+    assert call(rows=0) == sta.STA_OK
+    assert call(rows=0, x=None, y=None) == sta.STA_OK
+    assert call(rows=-1) == sta.STA_ERR_INVALID_ARG
+    assert call(n=12) == sta.STA_ERR_INVALID_ARG  # not a multiple of 8
+    assert call(n=0) == sta.STA_ERR_INVALID_ARG
+    assert call(n=16392) == sta.STA_ERR_INVALID_ARG  # past 16384
+    assert call(eps=0.0) == sta.STA_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == sta.STA_ERR_INVALID_ARG
+    assert call(eps=float("inf")) == sta.STA_ERR_INVALID_ARG
+    assert call(dtype=sta.STA_F32) == sta.STA_ERR_UNSUPPORTED
+    assert call(x=None) == sta.STA_ERR_INVALID_ARG
+    assert call(y=None) == sta.STA_ERR_INVALID_ARG
+    assert call(x=C.c_void_p((1 << 20) + 8)) == sta.STA_ERR_UNSUPPORTED  # 16-byte alignment
+    assert call(bias=C.c_void_p((1 << 20) + 4)) == sta.STA_ERR_UNSUPPORTED
+    assert call(gamma=C.c_void_p((1 << 20) + 12)) == sta.STA_ERR_UNSUPPORTED
