@@ -9,9 +9,12 @@
 // OT rows, and, when the caller asks for them, the block-wise kernel's column lists: the
 // union of the non-empty columns of the pair), and bitmap (one part tile per 64-thread
 // group: its 64 row words transposed into inner-tile words with warp shuffles).
+#include <algorithm>
 #include <vector>
 
 #include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
 
 namespace sta {
 namespace {
@@ -26,7 +29,8 @@ struct SrcDev {
 
 struct SrcBatch {
   SrcDev s[kMaxSrcPerLaunch];
-  int32_t h0;  // first mask head of this batch
+  int32_t hm[kMaxSrcPerLaunch];  // mask head of entry t (classify)
+  int32_t h0;                    // first mask head of this batch (bitmap: entries h0 .. h0 + n - 1)
 };
 
 // Bits lo..hi (clamped to 0..63) of a 64-bit word; 0 when the range is empty.
@@ -180,28 +184,63 @@ struct ScanOut {
 };
 
 // grid (R * ceil(C / 64), heads in batch), 256 threads: 64 outer tiles of one OT row per
-// block. Thread (g, u) reads rows g, g + 4, ... of tile column u (for bit-packed masks, 32
-// consecutive words of one row per warp) and keeps the popcount and the all-ones flag; the
-// four row groups are combined in shared memory. The row counts add up across blocks (the
-// counters are zeroed before the first launch) and the last block to finish scans them.
-__global__ void __launch_bounds__(kClassifyThreads) encode_classify_kernel(SrcBatch batch, int Lq, int Lk, int R,
+// block. Thread (g, u) takes rows g, g + 4, ... of tile column u and keeps the popcount and
+// the all-ones flag; the four row groups are combined in shared memory. The row counts add
+// up across blocks (the counters are zeroed before the first launch) and the last block to
+// finish scans them.
+//
+// kBulk (bit-packed sources whose rows start on 16 bytes and hold an even number of words):
+// the block's rows arrive in shared memory by one bulk copy each (no registers hold loads in
+// flight, so the whole tile row of 32 KB is requested at once) and the threads read them
+// from there. Otherwise every thread requests its row words itself (bit-packed: 16 at once).
+template <bool kBulk>
+__global__ void __launch_bounds__(kClassifyThreads, kBulk ? 6 : 4) encode_classify_kernel(SrcBatch batch, int Lq, int Lk, int R,
                                                                           int C, uint8_t* __restrict__ cls,
                                                                           int32_t* __restrict__ full_cnt,
                                                                           int32_t* __restrict__ part_cnt,
                                                                           unsigned long long* __restrict__ valid_cnt,
-                                                                          ScanOut so) {
+                                                                          ScanOut so, int* err) {
   const SrcDev& src = batch.s[blockIdx.y];
   const int CB = (C + kClassifyCols - 1) / kClassifyCols;
-  const int hm = batch.h0 + blockIdx.y, a = blockIdx.x / CB, cb = blockIdx.x % CB;
+  const int hm = batch.hm[blockIdx.y], a = blockIdx.x / CB, cb = blockIdx.x % CB;
   const int tid = threadIdx.x, lane = tid & 31, g = tid / kClassifyCols, u = tid % kClassifyCols;
   __shared__ int s_pop[kRowGroups][kClassifyCols];
   __shared__ int s_all[kRowGroups][kClassifyCols];
   __shared__ bool s_last;
-  const int c = cb * kClassifyCols + u;
+  const int c_beg = cb * kClassifyCols;
+  const int c = c_beg + u;
   const int i0 = a * STA_OT + g;
   int pop = 0;
   bool all = true;
-  if (c < C) {
+  if constexpr (kBulk) {
+    __shared__ __align__(128) uint64_t s_rows[STA_OT * kClassifyCols];
+    __shared__ __align__(8) uint64_t s_bar;
+    const int n_c = min(C, c_beg + kClassifyCols) - c_beg;  // even (C is even on this path)
+    const int rows = min(STA_OT, Lq - a * STA_OT);          // rows of this OT row inside the mask
+    const int64_t W = (Lk + 63) >> 6;
+    if (tid == 0) {
+      mbar_init(&s_bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) mbar_arrive_expect_tx(&s_bar, (uint32_t)(rows * n_c * 8));
+    if (tid < rows)
+      bulk_g2s(s_rows + tid * kClassifyCols,
+               static_cast<const uint64_t*>(src.data) + (int64_t)(a * STA_OT + tid) * W + c_beg, (uint32_t)(n_c * 8),
+               &s_bar);
+    const bool ok = mbar_wait(&s_bar, 0, err, 0x301);  // bounded; on timeout the counts are void
+    if (u < n_c) {
+      const int valid = Lk - c * STA_OT;  // columns of this word inside the mask
+      const uint64_t keep = valid < 64 ? (1ull << valid) - 1ull : ~0ull;
+#pragma unroll
+      for (int k = 0; k < kRowsPerThread; ++k) {
+        const int r = g + kRowGroups * k;
+        const uint64_t w = ok && r < rows ? s_rows[r * kClassifyCols + u] & keep : 0ull;
+        pop += __popcll(w);
+        all = all && w == ~0ull;
+      }
+    }
+  } else if (c < C) {
     if (src.kind == STA_MASK_DENSE_BITS) {  // every load of the thread in flight at once
       uint64_t rw[kRowsPerThread];
 #pragma unroll
@@ -476,12 +515,15 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
   unsigned long long* vcnt = (unsigned long long*)(ws + L.valid_cnt);
   long long* totals = (long long*)(ws + L.totals);
 
-  auto make_batch = [&](int h0, int n) {
+  // entries t = 0 .. n-1 take mask heads heads[t] (or h0 + t)
+  auto make_batch = [&](int h0, int n, const int* heads = nullptr) {
     SrcBatch b;
     memset(&b, 0, sizeof(b));
     b.h0 = h0;
     for (int t = 0; t < n; ++t) {
-      const sta_mask_src& s = srcs[h0 + t];
+      const int hm = heads ? heads[t] : h0 + t;
+      b.hm[t] = hm;
+      const sta_mask_src& s = srcs[hm];
       b.s[t].kind = s.kind;
       b.s[t].causal = s.causal;
       // |j - i| and j stay below 2^30: clamping to +-2^40 keeps every predicate and keeps the
@@ -502,11 +544,29 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
   so.full_row_ptr = out->full_row_ptr;
   so.part_row_ptr = out->part_row_ptr;
   so.totals = totals;
-  for (int h0 = 0; h0 < Hm; h0 += kMaxSrcPerLaunch) {
-    const int n = Hm - h0 < kMaxSrcPerLaunch ? Hm - h0 : kMaxSrcPerLaunch;
-    encode_classify_kernel<<<dim3((unsigned)(R * CB), (unsigned)n), kClassifyThreads, 0, st>>>(
-        make_batch(h0, n), Lq, Lk, (int)R, (int)C, cls, fcnt, pcnt, vcnt, so);
-    STA_LAUNCH_CHECK();
+  // classify: bit-packed heads whose rows can be bulk-copied (16-byte aligned rows of an even
+  // number of words) in one set of launches, every other head in another
+  int* err = device_error_word();
+  std::vector<int> bulk, other;
+  for (int h = 0; h < Hm; ++h) {
+    const sta_mask_src& s = srcs[h];
+    const bool b = s.kind == STA_MASK_DENSE_BITS && ((uintptr_t)s.data & 15) == 0 && (C & 1) == 0;
+    (b ? bulk : other).push_back(h);
+  }
+  for (int pass = 0; pass < 2; ++pass) {
+    const std::vector<int>& hs = pass == 0 ? bulk : other;
+    for (size_t t0 = 0; t0 < hs.size(); t0 += kMaxSrcPerLaunch) {
+      const int n = (int)std::min(hs.size() - t0, (size_t)kMaxSrcPerLaunch);
+      const dim3 grid((unsigned)(R * CB), (unsigned)n);
+      const SrcBatch b = make_batch(0, n, hs.data() + t0);
+      if (pass == 0)
+        encode_classify_kernel<true><<<grid, kClassifyThreads, 0, st>>>(b, Lq, Lk, (int)R, (int)C, cls, fcnt, pcnt,
+                                                                        vcnt, so, err);
+      else
+        encode_classify_kernel<false><<<grid, kClassifyThreads, 0, st>>>(b, Lq, Lk, (int)R, (int)C, cls, fcnt, pcnt,
+                                                                         vcnt, so, err);
+      STA_LAUNCH_CHECK();
+    }
   }
   out->n_mask_heads = Hm;
   out->Lq = Lq;

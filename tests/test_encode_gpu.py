@@ -140,3 +140,34 @@ def test_pattern_extremes_and_unaligned_bytes(dev, Lq, Lk):
     for key in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx", "part_bitmap"):
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
     _check_tile_lists(m, ref, len(heads), Lq, Lk)
+
+
+@pytest.mark.parametrize("Lq,Lk", [(130, 256), (300, 1000)])
+def test_bits_heads_with_and_without_bulk_rows(dev, Lq, Lk):
+    # bit-packed heads whose data start 16-byte aligned (rows copied in bulk) next to ones
+    # that start 8 bytes past it (rows read word by word), in one call
+    import torch
+
+    import split_kv_decode_bsr_gb300 as sta
+
+    u8 = [W.random_mask_u8(23, 7, Lq, Lk, dens, salt=s) for s, dens in enumerate((0.3, 0.02, 1.0, 0.6))]
+    u8[2][5:9] = 0
+    heads = [W.MaskHead("bits", data=W.pack_bits(x)) for x in u8]
+    ref = oracle.encode_mask(heads, Lq, Lk)
+    srcs = []
+    for t, hd in enumerate(heads):
+        words = torch.from_numpy(hd.data.view(np.int64))
+        if t % 2:
+            buf = torch.zeros(words.numel() + 2, dtype=torch.int64, device=dev)
+            view = buf[1:1 + words.numel()].view(words.shape)
+            view.copy_(words.to(dev))
+            assert view.data_ptr() % 16 == 8
+            srcs.append(sta.MaskSource.dense_bits(view))
+        else:
+            srcs.append(sta.MaskSource.dense_bits(words.to(dev)))
+    m = sta.sta_encode_mask(srcs, Lq, Lk)
+    got = m.host_arrays()
+    assert (got["n_full"], got["n_part"], got["n_valid"]) == (ref["n_full"], ref["n_part"], ref["n_valid"])
+    for key in ("full_row_ptr", "full_col_idx", "part_row_ptr", "part_col_idx", "part_bitmap"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    _check_tile_lists(m, ref, len(heads), Lq, Lk)
