@@ -530,6 +530,21 @@ def roofline_obj(bound, achieved, peak, unit, traffic, which):
             "traffic": traffic, "peak_source": which}
 
 
+def mha_roofline(b, t, peaks, traffic, which):
+    """The bound of a masked-MHA workload is the slower of its ideal times: valid-pair FLOPs at
+    the bf16 peak (tensor) or algorithmic bytes at the HBM peak (hbm); the line reports the
+    achieved rate against that one. Traffic (DRAM bytes) belongs to the hbm view only."""
+    t_tensor = b.flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = b.bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor > t_hbm:
+        r = roofline_obj("tensor", b.flops / t / 1e12, peaks["bf16_tflops"], "TFLOP/s", None, which)
+    else:
+        r = roofline_obj("hbm", b.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s", traffic, which)
+    r["algorithmic_bytes_per_launch"] = b.bytes
+    r["valid_pair_flops_per_launch"] = b.flops
+    return r
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -685,7 +700,7 @@ def main():
                            "kv_layout": f"paged, {db.page_size} tokens per page, random page order"
                            if db.page_size else "packed [T, Hkv, d]"},
                 "roofline": roofline_obj("hbm", db.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
-                                         recorded_traffic("decode.cu", "decode"), peak_src),
+                                         recorded_traffic("decode.cu", name), peak_src),
                 "e2e": {"value": db.kv_bytes / (e2e_s / steps) / 1e9, "unit": "GB/s",
                         "h2d_bytes_per_step": db.hq.numel() * 2,
                         "d2h_bytes_per_step": db.ho.numel() * 2 + db.hlse.numel() * 4},
@@ -705,8 +720,7 @@ def main():
                 "config": {"workload": b.wl.name, "valid_pairs": b.pairs, "kernel": b.kernel,
                            "split_kv": "planned" if b.split else "none", "workspace_bytes": b.ws.numel()},
                 "tensor_frac": tf / peaks["bf16_tflops"],
-                "roofline": roofline_obj("hbm", b.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
-                                         recorded_traffic(kf, name), peak_src),
+                "roofline": mha_roofline(b, t, peaks, recorded_traffic(kf, name), peak_src),
                 "gpu_launches": b.launches_per_step() * steps,
                 "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
             }
