@@ -155,3 +155,24 @@ def test_token_major_output_longformer_full_size(dev):
     # the 32-head, 16384-token workload (split heads included by the planner's choice)
     wl = W.longformer()
     _mha_pair(dev, wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, wl.Lq, wl.Lk, "auto", 0)
+
+
+def test_token_major_output_fp32_row_kernel(dev):
+    # the fp32 path (row-wise kernel only) writes token-major rows as well
+    import torch
+
+    import split_kv_decode_bsr_gb300 as sta
+
+    B, H, Lq, Lk, d = 2, 2, 70, 90, 64
+    q = W.make_tensor(61, 1, (B, H, Lq, d), "f32")
+    k = W.make_tensor(61, 2, (B, H, Lk, d), "f32")
+    v = W.make_tensor(61, 3, (B, H, Lk, d), "f32")
+    heads = [W.pattern(causal=True)]
+    mask = sta.sta_encode_mask(gpu_sources(heads, dev), Lq, Lk)
+    qd, kd, vd = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
+    o1, l1 = sta.sta_mha_fwd_splitkv(qd, kd, vd, mask, scale=0.125, kernel="row")
+    o2, l2 = sta.sta_mha_fwd_splitkv(qd, kd, vd, mask, scale=0.125, kernel="row", o_layout="blhd")
+    torch.cuda.synchronize()
+    assert torch.equal(o2.permute(0, 2, 1, 3), o1) and torch.equal(l1, l2)
+    o_ref, lse_ref = oracle.mha_fwd(q.f32, k.f32, v.f32, heads, [0, 0], 0.125)
+    compare(o1.cpu().numpy(), l1.cpu().numpy(), o_ref, lse_ref, "f32", "blhd f32")
