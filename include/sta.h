@@ -116,6 +116,33 @@ typedef struct {
   void* tile_lists;
 } sta_bsr_mask;
 
+/* sta_validate_mask -- check a two-level mask whose arrays are HOST copies
+ * (full_row_ptr, full_col_idx, part_row_ptr, part_col_idx, part_bitmap and, when
+ * set, tile_lists all point to host memory; head_tiles is ignored). Returns
+ * STA_OK when the mask is one that sta_encode_mask could have produced, else
+ * STA_ERR_INVALID_ARG with *failed_check (may be NULL) set to the first failed
+ * check:
+ *    1 shape fields < 1     2 ot_rows / ot_cols not ceil(L/64)
+ *    3 negative counts or too many tiles    4 a needed array is NULL
+ *    5 a row_ptr does not start at 0        6 a row_ptr decreases
+ *    7 a row_ptr does not end at n_full / n_part
+ *    8 a column outside [0, ot_cols)        9 columns of a row not ascending
+ *   10 a tile listed as both full and part 11 a full tile reaching past Lq or Lk
+ *   12 a part bitmap bit outside the mask  13 a part tile with no bit set
+ *   14 a part tile inside the mask with every bit set (a full tile)
+ *   15 n_valid (when >= 0) differs from the count of valid elements
+ *   16 tile_lists with ot_cols > 1024      17 a tile-list slot that is not the
+ *      union of its two outer-tile rows (columns ascending, kinds -1 / -2 / index)
+ * Host only (no CUDA call); cost linear in the mask's tiles and bitmap words.
+ * The kernels do not run these checks; given a mask that fails them they stay
+ * inside their buffers (CSR ranges clamped to n_full / n_part, columns and keys
+ * clamped into the mask, part indices checked against n_part) but compute wrong
+ * values, and the block-wise kernel, when it merges a damaged CSR itself, sets
+ * 0x213 in the device error word (sta_device_error). Likewise the decode kernels
+ * keep every request's token range inside the host copy's kv_indptr[n_req] and
+ * set 0x111 when the device copy disagrees. */
+sta_status sta_validate_mask(const sta_bsr_mask* mask, int* failed_check);
+
 /* Size in bytes of the tile_lists buffer for a mask of Hm heads over Lq x Lk
  * (see sta_bsr_mask), or 0 when Hm, Lq or Lk is < 1 or ceil(Lk/64) > 1024.
  * Host only. */

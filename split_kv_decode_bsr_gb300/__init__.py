@@ -38,7 +38,7 @@ STA_O_BHLD, STA_O_BLHD = 0, 1
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
 EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_fwd_layout",
-            "sta_bias_residual_layernorm", "sta_mha_select_kernel", "sta_decode_splitkv",
+            "sta_bias_residual_layernorm", "sta_validate_mask", "sta_mha_select_kernel", "sta_decode_splitkv",
             "sta_decode_splitkv_noalloc", "sta_decode_splitkv_paged", "sta_merge_lse", "sta_status_string", "sta_device_error",
             "sta_last_cuda_error", "sta_last_cuda_error_string")
 
@@ -89,6 +89,7 @@ def lib():
             h.sta_mha_fwd_layout.argtypes = [P, P, P, P, P, C.POINTER(_BsrMask), P, i32, i32, i32, i32, i32, i32, f32,
                                              i32, i32, i32, P, sz, P]
             h.sta_bias_residual_layernorm.argtypes = [P, P, P, P, P, P, P, C.c_int64, i32, f32, i32, P]
+            h.sta_validate_mask.argtypes = [C.POINTER(_BsrMask), C.POINTER(C.c_int)]
             h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
             h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
             h.sta_decode_splitkv_paged.argtypes = [P, P, P, i32, i32, P, P, P, P, i32, i32, i32, i32, i32, f32, i32,
@@ -208,6 +209,38 @@ class BsrMask:
                     part_row_ptr=self.part_row_ptr.cpu().numpy(), part_col_idx=self.part_col_idx.cpu().numpy(),
                     part_bitmap=self.part_bitmap.cpu().numpy().view("uint64").reshape(-1, 64),
                     n_full=self.n_full, n_part=self.n_part, n_valid=self.n_valid)
+
+    def validate(self) -> None:
+        """Copy the arrays to the host and run sta_validate_mask on them; raises StaError
+        (with .failed_check, the header's check number) when the mask is malformed."""
+        a = self.host_arrays()
+        tl = self.tile_lists.cpu().numpy() if self.tile_lists is not None else None
+        validate_mask_host(a, self.Hm, self.Lq, self.Lk, tile_lists=tl)
+
+
+def validate_mask_host(arrays: dict, Hm: int, Lq: int, Lk: int, tile_lists=None) -> None:
+    """sta_validate_mask on host numpy arrays (keys as BsrMask.host_arrays(); n_valid may be -1
+    to skip that check). Raises StaError with .failed_check set when a check fails."""
+    import numpy as np
+
+    keep = {k: np.ascontiguousarray(arrays[k], dtype=dt) for k, dt in
+            (("full_row_ptr", np.int32), ("full_col_idx", np.int32), ("part_row_ptr", np.int32),
+             ("part_col_idx", np.int32), ("part_bitmap", np.uint64))}
+    s = _BsrMask()
+    s.n_mask_heads, s.Lq, s.Lk = Hm, Lq, Lk
+    s.ot_rows, s.ot_cols = (Lq + 63) // 64, (Lk + 63) // 64
+    for k, v in keep.items():
+        setattr(s, k, v.ctypes.data if v.size else None)
+    s.full_row_ptr, s.part_row_ptr = keep["full_row_ptr"].ctypes.data, keep["part_row_ptr"].ctypes.data
+    s.n_full, s.n_part, s.n_valid = int(arrays["n_full"]), int(arrays["n_part"]), int(arrays.get("n_valid", -1))
+    tl = None if tile_lists is None else np.ascontiguousarray(tile_lists, dtype=np.uint8)
+    s.tile_lists = tl.ctypes.data if tl is not None else None
+    code = C.c_int(0)
+    st = lib().sta_validate_mask(C.byref(s), C.byref(code))
+    if st != STA_OK:
+        err = StaError("sta_validate_mask", st)
+        err.failed_check = code.value
+        raise err
 
 
 def _src_array(srcs: Sequence[MaskSource]):

@@ -139,7 +139,7 @@ sta_status mha_prepare(const sta_bsr_mask* mask, const int32_t* head_map, int B,
   if (which == STA_KERNEL_BLOCK && !block_kernel_supports(d, Lk, dtype)) return STA_ERR_UNSUPPORTED;
   a.mask = MaskView{mask->full_row_ptr, mask->full_col_idx, mask->part_row_ptr, mask->part_col_idx,
                     mask->part_bitmap, static_cast<const uint8_t*>(mask->tile_lists), mask->ot_rows, mask->ot_cols,
-                    mask->n_part};
+                    mask->n_part, mask->n_full};
   if (mask->tile_lists && (mask->ot_cols > kMaxTileListCols || ((uintptr_t)mask->tile_lists & 15)))
     return STA_ERR_INVALID_ARG;
   a.B = B; a.H = H; a.Lq = Lq; a.Lk = Lk; a.d = d; a.dtype = dtype;
@@ -235,6 +235,7 @@ sta_status decode_setup(const int32_t* indptr_host, int n_req, int Hq, int Hkv, 
   if ((int64_t)n_req * Hq > INT32_MAX / 2) return STA_ERR_INVALID_ARG;
   memset(&a, 0, sizeof(a));
   a.n_req = n_req; a.Hq = Hq; a.Hkv = Hkv; a.d = d;
+  a.T = (int)T;
   a.mode = num_splits == 0 ? 0 : 1;
   a.splits = num_splits;
   int dev = 0;

@@ -48,6 +48,7 @@ struct MaskView {
   const uint8_t* tile_lists;  // optional, see sta_bsr_mask::tile_lists
   int32_t ot_rows, ot_cols;
   int64_t n_part;              // part tiles (bounds the bitmap reads of the block-wise kernel)
+  int64_t n_full;              // full tiles (with n_part, bounds the CSR ranges the kernels read)
 };
 
 // Row r (0..63) of a part outer tile: 64-bit key mask, bit c = column c of the tile.

@@ -55,6 +55,19 @@ __device__ __forceinline__ int find_request(const int32_t* indptr, int n_req, in
   return lo;
 }
 
+// Request r's token range from the device copy of kv_indptr, kept non-decreasing and inside
+// [0, T] (the host copy's total): a device copy that disagrees with the host's reports 0x111
+// and cannot send a read past K / V.
+__device__ __forceinline__ void request_range(const DecodeArgs& A, int r, int& rb, int& re) {
+  rb = __ldg(A.kv_indptr + r);
+  re = __ldg(A.kv_indptr + r + 1);
+  if (rb < 0 || re < rb || re > A.T) {
+    record_error(A.err, 0x111);
+    rb = min(max(rb, 0), A.T);
+    re = min(max(re, rb), A.T);
+  }
+}
+
 template <int G, int D, int HB>
 __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const DecodeArgs A) {
   using Cfg = DecCfg<G, D, HB>;
@@ -88,7 +101,8 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
     auto pc_load = [&](int r, int base) {
       if (r != pc_r) {
         pc_r = r;
-        pc_rb = __ldg(A.kv_indptr + r);
+        int re_unused;
+        request_range(A, r, pc_rb, re_unused);  // the same clamped start the token ranges use
         pc_pb = __ldg(A.page_indptr + r);
         pc_pe = __ldg(A.page_indptr + r + 1);
       }
@@ -184,14 +198,15 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
       return true;
     };
     if (A.mode == 0) {
-      const int T = __ldg(A.kv_indptr + A.n_req);
+      const int T = min(__ldg(A.kv_indptr + A.n_req), A.T);
       const int start = blockIdx.x * A.range_len;
       const int end = min(T, start + A.range_len);
       if (start < end) {
         int r = find_request(A.kv_indptr, A.n_req, start);
         int a = start;
         while (a < end && r < A.n_req) {
-          const int rb = __ldg(A.kv_indptr + r), re = __ldg(A.kv_indptr + r + 1);
+          int rb, re;
+          request_range(A, r, rb, re);
           if (re <= a) { ++r; continue; }
           const int b = min(end, re);
           if (!emit_segment(r, a, b, a == rb && b == re, blockIdx.x + r)) break;
@@ -203,7 +218,9 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
       const int s = A.splits;
       for (int it = blockIdx.x; it < A.n_req * s; it += gridDim.x) {
         const int r = it / s, c = it % s;
-        const int rb = __ldg(A.kv_indptr + r), len = __ldg(A.kv_indptr + r + 1) - rb;
+        int rb, re;
+        request_range(A, r, rb, re);
+        const int len = re - rb;
         const int cl = (len + s - 1) / s;
         const int a = rb + min(len, c * cl), b = rb + min(len, (c + 1) * cl);
         if (!emit_segment(r, a, b, s == 1, it)) break;
@@ -369,7 +386,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs A) {
   const int64_t row = (int64_t)blockIdx.x * 8 + warp;
   if (row >= (int64_t)A.n_req * A.Hq) return;
   const int r = (int)(row / A.Hq), h = (int)(row % A.Hq);
-  const int beg = __ldg(A.kv_indptr + r), end = __ldg(A.kv_indptr + r + 1);
+  int beg, end;
+  request_range(A, r, beg, end);
   int slot0, s;
   if (end > beg) {
     if (A.mode == 0) {

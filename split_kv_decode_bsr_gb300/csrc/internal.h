@@ -69,6 +69,7 @@ struct DecodeArgs {
   float* part_o;    // [slots, Hq, d]
   float* part_lse;  // [slots, Hq]
   int n_req, Hq, Hkv, d;
+  int T;            // tokens (the host copy's kv_indptr[n_req]); device ranges are kept inside it
   float scale_log2;
   int mode;         // 0: balanced token ranges, 1: fixed splits per request
   int splits;       // mode 1: s

@@ -213,12 +213,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     n_cols = s_ncols;
   } else {
     {
-      const int fA0 = s_rowptr[0], fA1 = s_rowptr[1], pA0 = s_rowptr[2], pA1 = s_rowptr[3];
-      const int fB0 = s_rowptr[4], fB1 = s_rowptr[5], pB0 = s_rowptr[6], pB1 = s_rowptr[7];
-      for (int t = fA0 + threadIdx.x; t < fA1; t += kThreads) infoA[A.mask.full_col_idx[t]] = kFull;
-      for (int t = pA0 + threadIdx.x; t < pA1; t += kThreads) infoA[A.mask.part_col_idx[t]] = t;
-      for (int t = fB0 + threadIdx.x; t < fB1; t += kThreads) infoB[A.mask.full_col_idx[t]] = kFull;
-      for (int t = pB0 + threadIdx.x; t < pB1; t += kThreads) infoB[A.mask.part_col_idx[t]] = t;
+      // CSR ranges clamped to the arrays and columns checked against C: a damaged mask
+      // reports 0x213 instead of reaching past the buffers
+      const int64_t nf = A.mask.n_full, np = A.mask.n_part;
+      auto lo = [](int v) { return v < 0 ? 0 : v; };
+      const int fA0 = lo(s_rowptr[0]), fA1 = (int)min((int64_t)s_rowptr[1], nf);
+      const int pA0 = lo(s_rowptr[2]), pA1 = (int)min((int64_t)s_rowptr[3], np);
+      const int fB0 = lo(s_rowptr[4]), fB1 = (int)min((int64_t)s_rowptr[5], nf);
+      const int pB0 = lo(s_rowptr[6]), pB1 = (int)min((int64_t)s_rowptr[7], np);
+      auto put = [&](int32_t* info, int col, int32_t kind) {
+        if ((unsigned)col < (unsigned)C) info[col] = kind;
+        else record_error(A.err, 0x213);
+      };
+      for (int t = fA0 + threadIdx.x; t < fA1; t += kThreads) put(infoA, A.mask.full_col_idx[t], kFull);
+      for (int t = pA0 + threadIdx.x; t < pA1; t += kThreads) put(infoA, A.mask.part_col_idx[t], t);
+      for (int t = fB0 + threadIdx.x; t < fB1; t += kThreads) put(infoB, A.mask.full_col_idx[t], kFull);
+      for (int t = pB0 + threadIdx.x; t < pB1; t += kThreads) put(infoB, A.mask.part_col_idx[t], t);
     }
     __syncthreads();
     // Ascending list of the non-empty columns, built by all warps: one ballot per 32 columns,

@@ -8,6 +8,7 @@
 // running sum l, output rescaled by exp2(m_old - m_new)). Handles bf16 and fp32
 // inputs, head dims 64 and 128.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace sta {
 namespace {
@@ -120,8 +121,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   const float* sq = s_q[warp];
   const int a = i >> 6, r = i & 63;
   const int64_t mrow = (int64_t)hm * A.mask.ot_rows + a;
-  const int fb = A.mask.full_row_ptr[mrow], fe = A.mask.full_row_ptr[mrow + 1];
-  const int pb = A.mask.part_row_ptr[mrow], pe = A.mask.part_row_ptr[mrow + 1];
+  // CSR ranges clamped to the arrays (a damaged mask cannot send the loops past them)
+  const int fb = max(A.mask.full_row_ptr[mrow], 0), fe = (int)min((int64_t)A.mask.full_row_ptr[mrow + 1], A.mask.n_full);
+  const int pb = max(A.mask.part_row_ptr[mrow], 0), pe = (int)min((int64_t)A.mask.part_row_ptr[mrow + 1], A.mask.n_part);
 
   float m = -INFINITY, l = 0.f;
   float acc[E];
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
 
   // ---- full tiles: every key in range is valid
   for (int t = fb; t < fe; ++t) {
-    const int col = A.mask.full_col_idx[t];
+    // clamped into the mask like the part tiles' columns below
+    const int col = (int)min((unsigned)A.mask.full_col_idx[t], (unsigned)A.mask.ot_cols - 1u);
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
       const int64_t j0 = (int64_t)col * 64 + half * 32;
@@ -191,11 +194,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
       const int src = __ffs(nz) - 1;
       nz &= nz - 1;
       uint32_t bits = __shfl_sync(0xffffffffu, byte, src);
-      const int64_t base = (int64_t)__shfl_sync(0xffffffffu, col, src) * 64 + 8 * (src & 7);
+      // column and key clamped into the mask: a damaged mask (sta_validate_mask finds it)
+      // gives wrong values but no read outside K and V
+      const unsigned colv = min((unsigned)__shfl_sync(0xffffffffu, col, src), (unsigned)A.mask.ot_cols - 1u);
+      const int64_t base = (int64_t)colv * 64 + 8 * (src & 7);
       while (bits) {
         const int c = __ffs(bits) - 1;
         bits &= bits - 1;
-        const int64_t j = kv0 + base + c;
+        const int64_t j = kv0 + min(base + c, (int64_t)A.Lk - 1);
         float kd[E], vd[E];
         IO::load_lane(A.k, j, lane, kd);
         IO::load_lane(A.v, j, lane, vd);
