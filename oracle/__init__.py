@@ -23,6 +23,10 @@ it follows:
   transformer sub-layer's own: bias add, residual add, layer normalisation
   (mean and population variance over the row, eps inside the square root).
 
+* ``mla_decode`` -- decode against a shared latent KV cache (MLA in the weight-absorbed
+  form, one of the LLM subgraphs of the Cleave report's evaluation, section 評価結果): the
+  query heads score whole cached rows, the output sums the rows' latent part.
+
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, invariants, brute force and torch's float64
 ``scaled_dot_product_attention`` (for masks without empty rows). The analytic
@@ -33,6 +37,7 @@ rounding): parity unpinned, by design.
 from __future__ import annotations
 
 import ctypes as C
+import math
 import os
 import subprocess
 import threading
@@ -277,3 +282,32 @@ def bias_residual_layernorm(x, bias=None, residual=None, gamma=None, beta=None, 
     if beta is not None:
         y = y + np.asarray(beta, dtype=np.float64)
     return y, h
+
+
+def mla_decode(q, kv, kv_indptr, d_v: int = 512, scale=None):
+    """Decode against a shared latent KV cache (multi-head latent attention in the
+    weight-absorbed form; the Cleave report's evaluation, section 評価結果, lists MLA among the
+    LLM subgraphs it measures, and its Split operator applies to this reduction as to GQA's):
+    request r's query heads q[r, h] (length d_qk) score every cached row kv[t]
+    (length d_qk, the latent followed by the rotary key part) of tokens
+    kv_indptr[r] .. kv_indptr[r+1]-1, and the output is the softmax-weighted sum of the
+    rows' first d_v entries (the latent). fp64, two-pass softmax per (request, head).
+    Returns O [n_req, Hq, d_v] and the natural-log LSE [n_req, Hq] (empty request: 0, -inf)."""
+    q = np.asarray(q, dtype=np.float64)
+    kv = np.asarray(kv, dtype=np.float64)
+    n_req, Hq, dqk = q.shape
+    scale = 1.0 / math.sqrt(dqk) if scale is None else float(scale)
+    o = np.zeros((n_req, Hq, d_v))
+    lse = np.full((n_req, Hq), -np.inf)
+    for r in range(n_req):
+        b, e = int(kv_indptr[r]), int(kv_indptr[r + 1])
+        if e <= b:
+            continue
+        rows = kv[b:e]
+        s = (q[r] @ rows.T) * scale          # [Hq, len]
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        o[r] = (p @ rows[:, :d_v]) / l
+        lse[r] = (m + np.log(l))[:, 0]
+    return o, lse

@@ -467,3 +467,51 @@ def test_layernorm_normalised_moments():
     var = h.var(axis=-1)
     assert np.abs(y.mean(axis=-1)).max() < 1e-12
     assert np.abs((y ** 2).mean(axis=-1) - var / (var + eps)).max() < 1e-12
+
+
+# ---- decode against a shared latent KV cache (MLA)
+
+
+def test_mla_decode_with_full_values_is_mqa_decode():
+    # d_v = d_qk: values are the whole rows, i.e. single-KV-head decode with V = K, which the
+    # C oracle's GQA decode computes independently
+    rng = np.random.default_rng(7)
+    n_req, Hq, d = 3, 4, 64
+    ind = np.array([0, 5, 5, 40], dtype=np.int32)
+    q = rng.normal(size=(n_req, Hq, d)).astype(np.float32)  # the C oracle takes float32 inputs
+    kv = rng.normal(size=(40, d)).astype(np.float32)
+    o, lse = oracle.mla_decode(q, kv, ind, d_v=d, scale=0.2)
+    o2, lse2 = oracle.decode(q, kv[:, None, :], kv[:, None, :], ind, 1, 0.2)
+    assert np.abs(o - o2).max() < 1e-12
+    fin = np.isfinite(lse2)
+    assert np.array_equal(fin, np.isfinite(lse)) and np.abs(lse[fin] - lse2[fin]).max() < 1e-12
+    assert np.all(o[1] == 0) and np.all(lse[1] == -np.inf)  # the empty request
+
+
+def test_mla_decode_matches_torch_sdpa_fp64():
+    rng = np.random.default_rng(8)
+    Hq, dqk, dv, L = 16, 576, 512, 70
+    q = rng.normal(size=(1, Hq, dqk))
+    kv = rng.normal(size=(L, dqk))
+    o, lse = oracle.mla_decode(q, kv, np.array([0, L]), d_v=dv, scale=1 / math.sqrt(192))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q[0][:, None, :]), torch.from_numpy(kv)[None].expand(Hq, L, dqk),
+        torch.from_numpy(kv[:, :dv])[None].expand(Hq, L, dv), scale=1 / math.sqrt(192))
+    assert np.abs(o[0] - ref[:, 0, :].numpy()).max() < 1e-12
+    s = (q[0] @ kv.T) / math.sqrt(192)
+    assert np.abs(lse[0] - torch.logsumexp(torch.from_numpy(s), dim=1).numpy()).max() < 1e-12
+
+
+def test_mla_decode_single_token_and_constant_latent():
+    rng = np.random.default_rng(9)
+    q = rng.normal(size=(2, 16, 576))
+    kv = rng.normal(size=(9, 576))
+    # one cached token: O is its latent exactly, LSE its scaled score
+    o, lse = oracle.mla_decode(q[:1], kv[:1], np.array([0, 1]), scale=0.05)
+    assert np.array_equal(o[0], np.broadcast_to(kv[0, :512], (16, 512)))
+    assert np.abs(lse[0] - 0.05 * q[0] @ kv[0]).max() < 1e-12
+    # every token with the same latent (rope parts differ): O is that latent
+    kv2 = kv.copy()
+    kv2[:, :512] = kv[0, :512]
+    o, _ = oracle.mla_decode(q, kv2, np.array([0, 4, 9]), scale=0.05)
+    assert np.abs(o - kv[0, :512]).max() < 1e-12
