@@ -143,6 +143,39 @@ typedef struct {
  * set 0x111 when the device copy disagrees. */
 sta_status sta_validate_mask(const sta_bsr_mask* mask, int* failed_check);
 
+/* sta_mla_decode -- decode against a shared latent KV cache: multi-head latent
+ * attention in the weight-absorbed form (Cleave, 評価結果: MLA among the LLM
+ * subgraphs; the token reduction split into chunks and merged by log-sum-exp,
+ * Split演算子によるSplit-Kの対応):
+ *   O[r, h] = sum_t softmax_t(scale * q[r, h] . kv[t]) * kv[t, 0:512]
+ * over the tokens t of request r; LSE the natural-log normaliser.
+ *
+ *   q              [n_req, Hq, 576] bf16 (device): per query head a 512-entry
+ *                  latent part (the query taken into the latent space) then a
+ *                  64-entry rotary part
+ *   kv             [T, 576] bf16 (device): per cached token its 512-entry latent
+ *                  then its 64-entry rotary key, shared by every query head;
+ *                  request r owns rows kv_indptr[r] .. kv_indptr[r+1]-1
+ *   kv_indptr_dev  int32 [n_req+1] (device); kv_indptr_host: the same values
+ *                  (host), non-decreasing from 0 (else STA_ERR_INVALID_ARG); the
+ *                  kernels keep each device range inside kv_indptr_host[n_req]
+ *                  (0x111 in the device error word when the copies disagree)
+ *   Hq             a multiple of 16, at most 1024; scale > 0
+ *   chunk_tokens   0: the library picks; else tokens per chunk (rounded up to a
+ *                  multiple of 32): a request longer than a chunk is cut into
+ *                  chunks attended by their own CTAs, then merged by LSE
+ *   o              [n_req, Hq, 512] bf16 (device, written); lse [n_req, Hq] f32
+ *                  (device, written; may be NULL). An empty request gives O = 0,
+ *                  LSE = -inf.
+ *   workspace      device scratch (256-byte aligned) for the chunks' fp32
+ *                  partials, or NULL: *workspace_bytes is then set to the size
+ *                  needed and nothing is launched
+ * q, kv and o 16-byte aligned (else STA_ERR_UNSUPPORTED). One launch, plus a
+ * merge launch when some request is cut; asynchronous on `stream`. */
+sta_status sta_mla_decode(const void* q, const void* kv, const int32_t* kv_indptr_dev, const int32_t* kv_indptr_host,
+                          int n_req, int Hq, float scale, int chunk_tokens, void* o, float* lse, void* workspace,
+                          size_t* workspace_bytes, sta_stream stream);
+
 /* Size in bytes of the tile_lists buffer for a mask of Hm heads over Lq x Lk
  * (see sta_bsr_mask), or 0 when Hm, Lq or Lk is < 1 or ceil(Lk/64) > 1024.
  * Host only. */

@@ -38,7 +38,7 @@ STA_O_BHLD, STA_O_BLHD = 0, 1
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
 EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_fwd_layout",
-            "sta_bias_residual_layernorm", "sta_validate_mask", "sta_mha_select_kernel", "sta_decode_splitkv",
+            "sta_bias_residual_layernorm", "sta_validate_mask", "sta_mla_decode", "sta_mha_select_kernel", "sta_decode_splitkv",
             "sta_decode_splitkv_noalloc", "sta_decode_splitkv_paged", "sta_merge_lse", "sta_status_string", "sta_device_error",
             "sta_last_cuda_error", "sta_last_cuda_error_string")
 
@@ -90,6 +90,7 @@ def lib():
                                              i32, i32, i32, P, sz, P]
             h.sta_bias_residual_layernorm.argtypes = [P, P, P, P, P, P, P, C.c_int64, i32, f32, i32, P]
             h.sta_validate_mask.argtypes = [C.POINTER(_BsrMask), C.POINTER(C.c_int)]
+            h.sta_mla_decode.argtypes = [P, P, P, P, i32, i32, f32, i32, P, P, P, sz, P]
             h.sta_mha_select_kernel.argtypes = [C.POINTER(_BsrMask), i32, i32, i32, i32, i32, i32]
             h.sta_decode_splitkv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, i32, P, P, P, sz, P]
             h.sta_decode_splitkv_paged.argtypes = [P, P, P, i32, i32, P, P, P, P, i32, i32, i32, i32, i32, f32, i32,
@@ -388,6 +389,37 @@ def sta_mha_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask:
     have = C.c_size_t(workspace.numel())
     _check("sta_mha_fwd_layout", h.sta_mha_fwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), *args,
                                                       _ptr(workspace), C.byref(have), _stream(stream)))
+    return o, lse
+
+
+def mla_workspace_bytes(kv_indptr, n_req: int, Hq: int, chunk_tokens: int = 0) -> int:
+    n = C.c_size_t(0)
+    _check("sta_mla_decode", lib().sta_mla_decode(None, None, None, _indptr_host(kv_indptr), n_req, Hq, 1.0,
+                                                   chunk_tokens, None, None, None, C.byref(n), None))
+    return int(n.value)
+
+
+def sta_mla_decode(q: torch.Tensor, kv: torch.Tensor, kv_indptr_dev: torch.Tensor, kv_indptr_host, scale=None,
+                   chunk_tokens: int = 0, o=None, lse=None, workspace=None, stream=None):
+    """Decode against a shared latent KV cache: q [n_req, Hq, 576], kv [T, 576] bf16 (a 512-entry
+    latent then a 64-entry rotary part per row), kv_indptr int32 [n_req + 1]; returns
+    O [n_req, Hq, 512] bf16 and LSE [n_req, Hq] float32."""
+    n_req, Hq, dqk = q.shape
+    assert dqk == 576 and kv.dim() == 2 and kv.shape[1] == 576 and q.dtype == kv.dtype == torch.bfloat16
+    assert q.is_contiguous() and kv.is_contiguous()
+    scale = 1.0 / math.sqrt(192.0) if scale is None else float(scale)
+    if o is None:
+        o = torch.empty((n_req, Hq, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_req, Hq), dtype=torch.float32, device=q.device)
+    ind = _indptr_host(kv_indptr_host)
+    need = mla_workspace_bytes(kv_indptr_host, n_req, Hq, chunk_tokens)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    have = C.c_size_t(workspace.numel())
+    _check("sta_mla_decode", lib().sta_mla_decode(_ptr(q), _ptr(kv), _ptr(kv_indptr_dev), ind, n_req, Hq, scale,
+                                                   chunk_tokens, _ptr(o), _ptr(lse), _ptr(workspace), C.byref(have),
+                                                   _stream(stream)))
     return o, lse
 
 

@@ -438,6 +438,38 @@ def gqa_decode(seed: int = 0, n_req: int = 64, Hq: int = 32, Hkv: int = 8, d: in
 
 
 @dataclass
+class MlaWorkload:
+    name: str
+    n_req: int
+    Hq: int
+    d_qk: int
+    d_v: int
+    q: Tensor   # [n_req, Hq, d_qk]
+    kv: Tensor  # [T, d_qk]: the latent (first d_v entries) then the rotary key part
+    kv_indptr: np.ndarray  # int32 [n_req + 1]
+    scale: float
+
+
+def mla_decode(seed: int = 0, n_req: int = 64, Hq: int = 16, d_latent: int = 512, d_rope: int = 64,
+               lo: int = 512, hi: int = 32768, lengths=None, scale=None) -> MlaWorkload:
+    """Decode against a shared latent KV cache, DeepSeek-style shapes: a 512-entry latent plus a
+    64-entry rotary key per cached token, 16 query heads per GPU, ragged lengths drawn like the
+    GQA decode's. The scale defaults to 1/sqrt(128 + 64), the head size the weights are absorbed
+    from; q from the Q stream, the cache from the K stream (N(0,1), bf16)."""
+    lens = decode_lengths(seed, n_req, lo, hi) if lengths is None else np.asarray(lengths, np.int64)
+    indptr = np.zeros(n_req + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(lens)
+    T = int(indptr[-1])
+    assert T < 2**31
+    d_qk = d_latent + d_rope
+    q = make_tensor(seed, STREAM_Q, (n_req, Hq, d_qk), "bf16")
+    kv = make_tensor(seed, STREAM_K, (T, d_qk), "bf16")
+    sc = 1.0 / math.sqrt(128 + d_rope) if scale is None else float(scale)
+    return MlaWorkload(f"mla-decode bf16 n_req{n_req} Hq{Hq} latent{d_latent}+rope{d_rope} T{T}", n_req, Hq, d_qk,
+                       d_latent, q, kv, indptr.astype(np.int32), sc)
+
+
+@dataclass
 class PagedKV:
     page_size: int
     k_pages: Tensor        # [n_pages, page_size, Hkv, d]
