@@ -362,6 +362,45 @@ class DecodeBench:
         return 2
 
 
+class MlaBench:
+    """Decode against a shared latent KV cache (64 requests, 16 query heads, 512 + 64 entries per
+    cached token, lengths 512..32768 like the GQA decode)."""
+
+    def __init__(self, dev):
+        import torch
+
+        import split_kv_decode_bsr_gb300 as sta
+        import workloads as W
+
+        self.sta = sta
+        self.wl = wl = W.mla_decode()
+        self.q, self.kv = host_tensor(wl.q).to(dev), host_tensor(wl.kv).to(dev)
+        self.ind_host = wl.kv_indptr
+        self.ind = torch.from_numpy(wl.kv_indptr).to(dev)
+        self.T = int(wl.kv_indptr[-1])
+        self.kv_bytes = self.T * wl.d_qk * 2
+        self.bytes = self.kv_bytes + wl.n_req * wl.Hq * (wl.d_qk + wl.d_v) * 2 + wl.n_req * wl.Hq * 4
+        self.flops = 2 * wl.Hq * self.T * (wl.d_qk + wl.d_v)
+        self.o = torch.empty((wl.n_req, wl.Hq, wl.d_v), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((wl.n_req, wl.Hq), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(max(sta.mla_workspace_bytes(self.ind_host, wl.n_req, wl.Hq), 256), dtype=torch.uint8,
+                              device=dev)
+        self.hq = self.q.cpu().pin_memory()
+        self.ho = torch.empty_like(self.o, device="cpu").pin_memory()
+
+    def step(self):
+        self.sta.sta_mla_decode(self.q, self.kv, self.ind, self.ind_host, scale=self.wl.scale, o=self.o, lse=self.lse,
+                                workspace=self.ws)
+
+    def step_e2e(self):  # the latent cache stays resident; query tokens in, outputs out
+        self.q.copy_(self.hq, non_blocking=True)
+        self.step()
+        self.ho.copy_(self.o, non_blocking=True)
+
+    def launches_per_step(self):
+        return 2  # decode (+ the merge of the requests cut into chunks)
+
+
 class EpilogueBench:
     """The fused bias + residual + layer norm after the output projection of a 16384-token,
     32-head x 128 attention layer: x, residual [16384, 4096] bf16, bias [4096] bf16,
@@ -553,9 +592,9 @@ def main():
     ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
     ap.add_argument("--workload", default="bert-band")
     ap.add_argument("--extra", default="bigbird,longformer,decode,decode-paged,long-causal,causal-1head,sparse-random,"
-                                       "epilogue-ln,mha-token-major",
+                                       "epilogue-ln,mha-token-major,mla-decode",
                     help="comma list of secondary workloads (bigbird, longformer, decode, decode-paged, long-causal, "
-                         "causal-1head, sparse-random, epilogue-ln, mha-token-major) or 'none'")
+                         "causal-1head, sparse-random, epilogue-ln, mha-token-major, mla-decode) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")
@@ -660,6 +699,26 @@ def main():
                 "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
             }
             del eb
+            continue
+        if name == "mla-decode":
+            mb2 = MlaBench(dev)
+            g = graphed(mb2.step)
+            ms, _ = time_device(g, steps, args.warmup, dist, flush)
+            t = sum(ms) / len(ms) / 1e3
+            e2e_s = time_e2e(mb2.step_e2e, steps, args.warmup, dist)
+            extras[name] = {
+                "metric": "MLA decode KV-read GB/s", "value": mb2.kv_bytes / t / 1e9, "unit": "GB/s",
+                "ms_per_step": 1e3 * t, "tflops": mb2.flops / t / 1e12,
+                "config": {"workload": mb2.wl.name, "T": mb2.T, "kv_bytes": mb2.kv_bytes, "chunking": "library",
+                           "kernel": "mma.sync m16n8k16 bf16 (16 query heads as M)"},
+                "roofline": roofline_obj("hbm", mb2.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
+                                         recorded_traffic("mla.cu", name), peak_src),
+                "e2e": {"value": mb2.kv_bytes / (e2e_s / steps) / 1e9, "unit": "GB/s",
+                        "h2d_bytes_per_step": mb2.hq.numel() * 2, "d2h_bytes_per_step": mb2.ho.numel() * 2},
+                "gpu_launches": mb2.launches_per_step() * steps,
+                "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
+            }
+            del mb2
             continue
         if name == "mha-token-major":
             b = MhaBench("longformer", dev, args.mha_splits)

@@ -39,7 +39,9 @@ constexpr int kStages = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kHeads * kRowBytes;                 // 18,688
 constexpr int kOffS = kOffKV + kStages * kTile * kRowBytes;        // + 74,752
-constexpr int kSmemBytes = kOffS + kWarps * kHeads * kTile * 4;    // + 8,192 = 101,632
+constexpr int kSRow = kTile + 8;  // partial-score row stride in floats: 8-byte accesses of a
+                                   // half-warp (rows g..g+3) fall in distinct banks
+constexpr int kSmemBytes = kOffS + kWarps * kHeads * kSRow * 4;    // + 10,240 = 103,680
 
 struct MlaArgs {
   const __nv_bfloat16* q;   // [n_req, Hq, 576]
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
 #pragma unroll
   for (int i = 0; i < kNbDv; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g and g + 8
-  float* s_part = reinterpret_cast<float*>(smem + kOffS);      // [warp][16][32]
+  float* s_part = reinterpret_cast<float*>(smem + kOffS);      // [warp][16][kSRow]
 
   for (int k = 0; ok && k < ntiles; ++k) {
     const int s = k % kStages;
@@ -190,9 +192,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
     }
 #pragma unroll
     for (int nb = 0; nb < 4; ++nb) {
-      float* sp = s_part + warp * kHeads * kTile;
-      *reinterpret_cast<float2*>(sp + g * kTile + 8 * nb + 2 * t) = make_float2(sacc[nb][0], sacc[nb][1]);
-      *reinterpret_cast<float2*>(sp + (g + 8) * kTile + 8 * nb + 2 * t) = make_float2(sacc[nb][2], sacc[nb][3]);
+      float* sp = s_part + warp * kHeads * kSRow;
+      *reinterpret_cast<float2*>(sp + g * kSRow + 8 * nb + 2 * t) = make_float2(sacc[nb][0], sacc[nb][1]);
+      *reinterpret_cast<float2*>(sp + (g + 8) * kSRow + 8 * nb + 2 * t) = make_float2(sacc[nb][2], sacc[nb][3]);
     }
     __syncthreads();
     // ---- full scores at this thread's fragment positions (rows g, g + 8; 8 tokens each)
@@ -203,9 +205,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
       float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float* sp = s_part + w * kHeads * kTile;
-        const float2 x = *reinterpret_cast<const float2*>(sp + g * kTile + 8 * nb + 2 * t);
-        const float2 y = *reinterpret_cast<const float2*>(sp + (g + 8) * kTile + 8 * nb + 2 * t);
+        const float* sp = s_part + w * kHeads * kSRow;
+        const float2 x = *reinterpret_cast<const float2*>(sp + g * kSRow + 8 * nb + 2 * t);
+        const float2 y = *reinterpret_cast<const float2*>(sp + (g + 8) * kSRow + 8 * nb + 2 * t);
         a.x += x.x; a.y += x.y; b.x += y.x; b.y += y.y;
       }
       const int j = 8 * nb + 2 * t;
@@ -371,15 +373,27 @@ extern "C" sta_status sta_mla_decode(const void* q, const void* kv, const int32_
   const int64_t T = kv_indptr_host[n_req];
   // tokens per chunk: given (rounded up to the tile), or about 2 CTAs' share per SM of the
   // whole token stream across all head groups, at least 4 tiles
+  auto count_items = [&](int ch) {
+    int64_t n = 0;
+    for (int x = 0; x < n_req; ++x) {
+      const int len = kv_indptr_host[x + 1] - kv_indptr_host[x];
+      n += len > ch ? (len + ch - 1) / ch : 1;
+    }
+    return n;
+  };
   int chunk = chunk_tokens;
   if (chunk == 0) {
+    // the smallest chunk (a multiple of the tile, at least 4 tiles) whose items across all head
+    // groups fit one wave of resident CTAs (two per SM): a second, partial wave would run a
+    // full chunk after the first
     int dev = 0, sms = 0;
     STA_CUDA_TRY(cudaGetDevice(&dev));
     STA_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const int64_t slots = (int64_t)sms * 2;
-    const int64_t hg = Hq / kHeads;
-    int64_t per = (T * hg + slots - 1) / slots;
-    chunk = (int)std::max<int64_t>(4 * kTile, std::min<int64_t>(per, 1 << 20));
+    const int64_t slots = (int64_t)sms * 2, hg = Hq / kHeads;
+    int64_t ch = std::max<int64_t>(4 * kTile, (T * hg + slots - 1) / slots);
+    ch = (ch + kTile - 1) / kTile * kTile;
+    while (ch < (1 << 30) && count_items((int)ch) * hg > slots) ch += std::max<int64_t>(kTile, ch / 32 / kTile * kTile);
+    chunk = (int)std::min<int64_t>(ch, 1 << 30);
   }
   chunk = (chunk + kTile - 1) / kTile * kTile;
   int64_t items = 0, split_items = 0;
