@@ -236,3 +236,27 @@ def test_layernorm_rejects_bad_arguments_on_host(lib):
     assert call(x=C.c_void_p((1 << 20) + 8)) == sta.STA_ERR_UNSUPPORTED  # 16-byte alignment
     assert call(bias=C.c_void_p((1 << 20) + 4)) == sta.STA_ERR_UNSUPPORTED
     assert call(gamma=C.c_void_p((1 << 20) + 12)) == sta.STA_ERR_UNSUPPORTED
+
+
+def test_mla_decode_host_checks(lib):
+    ind = (C.c_int32 * 4)(0, 100, 100, 5000)
+    n = C.c_size_t(0)
+
+    def call(Hq=16, chunk=0, scale=0.07, indptr=ind, n_req=3):
+        return lib.sta_mla_decode(None, None, None, indptr, n_req, Hq, scale, chunk, None, None, None, C.byref(n),
+                                  None)
+
+    # chunks of 64 tokens: request 0 (100 tokens) is cut into 2 chunks, request 2 (4900) into
+    # 77, the empty request 1 runs as one item
+    assert call(chunk=64) == sta.STA_OK
+    items = 2 + 1 + (4900 + 63) // 64
+    assert n.value == ((items * 16 * 512 * 4 + 255) // 256) * 256 + ((items * 16 * 4 + 255) // 256) * 256
+    assert call(chunk=100000) == sta.STA_OK and n.value == 256  # nothing cut: no partials
+    assert call(Hq=24) == sta.STA_ERR_INVALID_ARG  # not a multiple of 16
+    assert call(Hq=0) == sta.STA_ERR_INVALID_ARG
+    assert call(scale=0.0) == sta.STA_ERR_INVALID_ARG
+    assert call(chunk=-1) == sta.STA_ERR_INVALID_ARG
+    bad = (C.c_int32 * 4)(0, 100, 50, 5000)  # decreasing
+    assert call(indptr=bad) == sta.STA_ERR_INVALID_ARG
+    bad0 = (C.c_int32 * 4)(3, 100, 100, 5000)  # not starting at 0
+    assert call(indptr=bad0) == sta.STA_ERR_INVALID_ARG
