@@ -29,7 +29,8 @@ namespace {
 constexpr int kDqk = 576, kDv = 512;
 constexpr int kHeads = 16;                    // query heads per CTA: the M of one mma
 constexpr int kTile = 32;                     // tokens per tile
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;                     // consumer warps; warp kWarps issues the copies
+constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kRowBytes = kDqk * 2 + 16;      // padded shared-memory row (1168 bytes)
 constexpr int kKsteps = kDqk / 16;            // 36 k-steps of the score product
 constexpr int kKstepsPerWarp = kKsteps / kWarps;  // 9
@@ -103,9 +104,9 @@ __device__ __forceinline__ void mla_item(const MlaArgs& A, int item, int& r, int
 }
 
 // grid (items, Hq / 16), 128 threads, kSmemBytes of dynamic shared memory.
-__global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) mla_decode_kernel(const MlaArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kStages], q_full;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], q_full;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
   int r, c, nc, first;
@@ -123,30 +124,36 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
   for (int i = threadIdx.x; i < kStages * kTile * kRowBytes / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + kOffKV)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);  // one arrival per consumer warp once it has read the stage
+    }
     mbar_init(&q_full, 1);
     fence_mbar_init();
   }
   fence_proxy_async_smem();  // the zero stores come before any bulk copy into those rows
   __syncthreads();
-  // warp 0: the 16 query rows, then the first tiles; lane i copies row i
-  auto issue_tile = [&](int k) {  // warp 0 only
-    if (k >= ntiles) return;
-    const int s = k % kStages, base = t0 + k * kTile, n = min(kTile, t1 - base);
-    if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(n * kDqk * 2));
-    __syncwarp();
-    if (lane < n)
-      bulk_g2s(smem + kOffKV + (s * kTile + lane) * kRowBytes, A.kv + (int64_t)(base + lane) * kDqk,
-               (uint32_t)(kDqk * 2), &full[s]);
-  };
-  if (warp == 0) {
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- copies (lane i: row i)
     if (lane == 0) mbar_arrive_expect_tx(&q_full, (uint32_t)(kHeads * kDqk * 2));
     __syncwarp();
     if (lane < kHeads)
       bulk_g2s(smem + kOffQ + lane * kRowBytes, A.q + ((int64_t)r * A.Hq + hg * kHeads + lane) * kDqk,
                (uint32_t)(kDqk * 2), &q_full);
-    issue_tile(0);
-    issue_tile(1);
+    for (int k = 0; k < ntiles; ++k) {
+      const int s = k % kStages, base = t0 + k * kTile, n = min(kTile, t1 - base);
+      // the stage is free once every consumer warp has finished tile k - kStages
+      // lane 0 waits, the warp follows its answer (no lane leaves the loop alone)
+      bool free_ok = true;
+      if (lane == 0) free_ok = mbar_wait(&empty[s], ((uint32_t)(k / kStages) & 1u) ^ 1u, A.err, 0x504);
+      if (!__shfl_sync(0xffffffffu, free_ok, 0)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(n * kDqk * 2));
+      __syncwarp();
+      if (lane < n)
+        bulk_g2s(smem + kOffKV + (s * kTile + lane) * kRowBytes, A.kv + (int64_t)(base + lane) * kDqk,
+                 (uint32_t)(kDqk * 2), &full[s]);
+    }
+    return;
   }
   const bool q_ok = mbar_wait(&q_full, 0, A.err, 0x501);
   bool ok = q_ok;
@@ -165,13 +172,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g and g + 8
   float* s_part = reinterpret_cast<float*>(smem + kOffS);      // [warp][16][kSRow]
 
-  for (int k = 0; ok && k < ntiles; ++k) {
+  // Every consumer warp runs every tile and reaches every barrier: after a timed-out wait
+  // (error word set) the warps stop waiting and compute on whatever the stages hold, so that
+  // none is left alone at a named barrier.
+  for (int k = 0; k < ntiles; ++k) {
     const int s = k % kStages;
-    if (!mbar_wait(&full[s], (uint32_t)(k / kStages) & 1u, A.err, 0x502)) {
-      ok = false;
-      break;
+    if (ok) {  // every lane waits (each then sees the copied rows); the warp follows lane 0
+      const bool got = mbar_wait(&full[s], (uint32_t)(k / kStages) & 1u, A.err, 0x502);
+      ok = __shfl_sync(0xffffffffu, got, 0);
     }
-    consumed = k + 1;
+    if (ok) consumed = k + 1;
     const uint32_t kvs = sbase + kOffKV + s * kTile * kRowBytes;
     // ---- partial scores over this warp's dimensions, 4 n-blocks of 8 tokens
     float sacc[4][4];
@@ -196,7 +206,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
       *reinterpret_cast<float2*>(sp + g * kSRow + 8 * nb + 2 * t) = make_float2(sacc[nb][0], sacc[nb][1]);
       *reinterpret_cast<float2*>(sp + (g + 8) * kSRow + 8 * nb + 2 * t) = make_float2(sacc[nb][2], sacc[nb][3]);
     }
-    __syncthreads();
+    named_bar_sync(1, kWarps * 32);  // every consumer warp's partial scores are in
     // ---- full scores at this thread's fragment positions (rows g, g + 8; 8 tokens each)
     const int nvalid = min(kTile, ntok - k * kTile);
     float sv[4][4];
@@ -277,13 +287,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2) mla_decode_kernel(const MlaArg
         mma_bf16(oacc[nbd + 1], pa[ks], b[2], b[3]);
       }
     }
-    __syncthreads();  // stage s and the partial scores are free again
-    if (warp == 0) issue_tile(k + kStages);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
+    named_bar_sync(2, kWarps * 32);         // the partial scores may be overwritten
   }
   if (!ok && threadIdx.x == 0) {
-    // after a timed-out wait: the copies still in flight land before shared memory is released
+    // after a timed-out wait: the last copy of each stage (issued once the consumers released
+    // the stage) lands before shared memory is released; every wait is bounded
     if (!q_ok) mbar_wait(&q_full, 0, A.err, 0x503);
-    for (int k = consumed; k < min(consumed + kStages, ntiles); ++k)
+    for (int k = max(consumed, ntiles - kStages); k < ntiles; ++k)
       mbar_wait(&full[k % kStages], (uint32_t)(k / kStages) & 1u, A.err, 0x503);
   }
   // ---- epilogue: the row sums, then O / l and the LSE (rows without a valid token: 0, -inf)
@@ -431,7 +443,7 @@ extern "C" sta_status sta_mla_decode(const void* q, const void* kv, const int32_
   a.err = device_error_word();
   cudaStream_t st = (cudaStream_t)stream;
   STA_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-  mla_decode_kernel<<<dim3((unsigned)items, (unsigned)(Hq / kHeads)), kWarps * 32, kSmemBytes, st>>>(a);
+  mla_decode_kernel<<<dim3((unsigned)items, (unsigned)(Hq / kHeads)), kThreads, kSmemBytes, st>>>(a);
   STA_LAUNCH_CHECK();
   if (split_items) {
     mla_merge_kernel<<<(unsigned)(((int64_t)n_req * Hq + 7) / 8), 256, 0, st>>>(a);
