@@ -7,15 +7,17 @@
 // softmax-weighted sum of the rows' latent parts (their first 512 entries). One KV head for all
 // query heads, the values inside the keys.
 //
-// One CTA per (chunk of one request's tokens, group of 16 query heads), 4 warps. The 16 heads
-// are the M of mma.sync.m16n8k16 (bf16 operands, fp32 accumulators): the scores S[16 x 32
-// tokens] of a tile are split across the warps by head dimension (a warp keeps its 144
-// dimensions of the 16 query rows in registers and adds its partial S into shared memory),
-// every warp then turns the summed S into the weights P, and P.V is split by output dimension
-// (128 latent entries per warp, accumulators in registers). Cached rows arrive by one bulk copy
-// per row into shared-memory rows padded to 1168 bytes (so that the eight rows an ldmatrix reads
-// fall in distinct banks), two tiles of 32 tokens in flight; the latent part of the same rows is
-// the V operand (ldmatrix .trans), so each cached row is read from HBM once per head group.
+// One CTA per (chunk of one request's tokens, group of 16 query heads): four compute warps and
+// a warp that issues the copies. The 16 heads are the M of mma.sync.m16n8k16 (bf16 operands,
+// fp32 accumulators): the scores S[16 x 32 tokens] of a tile are split across the compute warps
+// by head dimension (a warp keeps its 144 dimensions of the 16 query rows in registers and adds
+// its partial S into shared memory), every compute warp then turns the summed S into the
+// weights P, and P.V is split by output dimension (128 latent entries per warp, accumulators in
+// registers). Cached rows arrive by one bulk copy per row into shared-memory rows padded to 1168
+// bytes (so that the eight rows an ldmatrix reads fall in distinct banks), two tiles of 32
+// tokens in flight; the copy warp refills a stage once every compute warp has released it. The
+// latent part of the same rows is the V operand (ldmatrix .trans), so each cached row is read
+// from HBM once per head group.
 #include <algorithm>
 #include <cmath>
 
