@@ -91,18 +91,62 @@ __device__ __forceinline__ void mla_range(const MlaArgs& A, int r, int& rb, int&
 }
 __device__ __forceinline__ int mla_chunks(int len, int chunk) { return len > chunk ? (len + chunk - 1) / chunk : 1; }
 
-// Item `item` -> request r, its chunk c, the request's chunk count and its first item.
+// Item `item` -> request r, its chunk c, the request's chunk count and its first item, found
+// by a whole warp 32 requests at a time (chunk counts prefix-summed with shuffles); r = n_req
+// when the item lies past the last request. Every lane returns the same values.
 __device__ __forceinline__ void mla_item(const MlaArgs& A, int item, int& r, int& c, int& nc, int& first) {
+  const int lane = threadIdx.x & 31;
   int base = 0;
-  for (r = 0; r < A.n_req; ++r) {
-    int rb, re;
-    mla_range(A, r, rb, re);
-    nc = mla_chunks(re - rb, A.chunk);
-    if (item < base + nc) break;
-    base += nc;
+  for (int r0 = 0; r0 < A.n_req; r0 += 32) {
+    const int x = r0 + lane;
+    int n = 0;
+    if (x < A.n_req) {
+      int rb, re;
+      mla_range(A, x, rb, re);
+      n = mla_chunks(re - rb, A.chunk);
+    }
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (item < base + total) {
+      const int L = __ffs(__ballot_sync(0xffffffffu, item < base + incl)) - 1;  // first lane past the item
+      r = r0 + L;
+      nc = __shfl_sync(0xffffffffu, n, L);
+      first = base + __shfl_sync(0xffffffffu, incl, L) - nc;
+      c = item - first;
+      return;
+    }
+    base += total;
   }
-  c = item - base;
+  r = A.n_req;
+  c = 0;
+  nc = 1;
   first = base;
+}
+
+// First item and chunk count of request r (whole warp, 32 requests at a time).
+__device__ __forceinline__ void mla_request_items(const MlaArgs& A, int r, int& first, int& nc) {
+  const int lane = threadIdx.x & 31;
+  first = 0;
+  for (int r0 = 0; r0 < r; r0 += 32) {
+    const int x = r0 + lane;
+    int n = 0;
+    if (x < r) {
+      int rb, re;
+      mla_range(A, x, rb, re);
+      n = mla_chunks(re - rb, A.chunk);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    first += n;
+  }
+  int rb, re;
+  mla_range(A, r, rb, re);
+  nc = mla_chunks(re - rb, A.chunk);
 }
 
 // grid (items, Hq / 16), 128 threads, kSmemBytes of dynamic shared memory.
@@ -346,13 +390,8 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaArgs A) {
   const int64_t row = (int64_t)blockIdx.x * 8 + warp;
   if (row >= (int64_t)A.n_req * A.Hq) return;
   const int r = (int)(row / A.Hq), h = (int)(row % A.Hq);
-  int first = 0, nc = 1;
-  for (int x = 0; x <= r; ++x) {
-    int rb, re;
-    mla_range(A, x, rb, re);
-    nc = mla_chunks(re - rb, A.chunk);
-    if (x < r) first += nc;
-  }
+  int first, nc;
+  mla_request_items(A, r, first, nc);
   if (nc == 1) return;  // written by the decode kernel
   if (first + nc > A.items) {  // device and host kv_indptr disagree: no read past the partials
     record_error(A.err, 0x111);
