@@ -23,7 +23,7 @@ timed region.
 workload: the reference arm of this comparison is the plain restatement of
 the method, not a GPU system.
 
-Multi-GPU: the path shards into independent units but this build runs
+Multi-GPU: the path shards into independent units and the bench runs
 replicas only (every rank runs the same workload on its own GPU); value is
 the sum over ranks divided by the slowest rank's time.
 """

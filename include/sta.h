@@ -1,7 +1,8 @@
 /*
  * sta.h -- C ABI of libsta: masked multi-head attention over a two-level
- * (BSR + bitmap) mask, and split-KV decode with a log-sum-exp merge, for
- * NVIDIA GB300 (sm_103a).
+ * (BSR + bitmap) mask, split-KV decode (GQA over packed or paged KV, and
+ * against a shared latent KV cache) with a log-sum-exp merge, and the fused
+ * operators that follow the attention, for NVIDIA GB300 (sm_103a).
  *
  * Sources of the operations:
  *  - "Accelerating Sparse Transformer Inference on GPU" (STOF):
@@ -12,10 +13,13 @@
  *      デュアルカーネル戦略 / カーネル選択 -- a row-wise kernel for short, highly
  *      sparse cases, a block-wise kernel for the general case, and an analytic
  *      model that picks between them.
+ *      演算子融合モジュール -- fusion of the MHA layer with the operators after
+ *      it (here by a fixed rule: sta_mha_fwd_layout, sta_bias_residual_layernorm).
  *  - "Cleave: Scaling Tensor Program Optimization via Decoupled Algebraic
  *    Search and Operator Scheduling": Split演算子によるSplit-Kの対応 and the
  *    abstract -- a Split operator with split count s parallelises a reduction
- *    dimension (FlashDecoding); the partial softmax results are merged.
+ *    dimension (FlashDecoding); the partial softmax results are merged;
+ *    評価結果 -- MLA among the measured LLM subgraphs (sta_mla_decode).
  *
  * Conventions (the pages leave these open; plainest readings):
  *  - Q, K, V, O are [B, H, L, d] row-major, d innermost (decode: Q/O
@@ -49,7 +53,7 @@ extern "C" {
 typedef int sta_status;
 #define STA_OK 0
 #define STA_ERR_INVALID_ARG 1  /* null pointer, bad size, inconsistent arguments */
-#define STA_ERR_UNSUPPORTED 2  /* dtype / head dim / alignment this build does not handle */
+#define STA_ERR_UNSUPPORTED 2  /* dtype / head dim / alignment the library does not handle */
 #define STA_ERR_WORKSPACE 3    /* workspace missing or too small */
 #define STA_ERR_CUDA 4         /* the CUDA runtime reported an error */
 
