@@ -46,6 +46,7 @@ BIG = 1 << 40
 
 
 class StaError(RuntimeError):
+    """A library call returned a status other than STA_OK (.status holds it)."""
     def __init__(self, fn: str, status: int):
         self.status = status
         msg = f"{fn} failed: {status_string(status)} ({status})"
@@ -111,6 +112,7 @@ def lib():
 
 
 def status_string(status: int) -> str:
+    """The library's message for a status code."""
     return lib().sta_status_string(int(status)).decode()
 
 
@@ -303,6 +305,7 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
 
 
 def sta_mha_select_kernel(mask: BsrMask, B: int, H: int, d: int, dtype=torch.bfloat16) -> str:
+    """Which kernel sta_mha_fwd would run under kernel="auto": "block" or "row" (host only)."""
     s = mask.struct()
     r = lib().sta_mha_select_kernel(C.byref(s), B, H, mask.Lq, mask.Lk, d, _dtype_code(dtype))
     if r < 0:
@@ -393,6 +396,7 @@ def sta_mha_fwd_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask:
 
 
 def mla_workspace_bytes(kv_indptr, n_req: int, Hq: int, chunk_tokens: int = 0) -> int:
+    """Workspace size sta_mla_decode needs for these requests (host only, never 0)."""
     n = C.c_size_t(0)
     _check("sta_mla_decode", lib().sta_mla_decode(None, None, None, _indptr_host(kv_indptr), n_req, Hq, 1.0,
                                                    chunk_tokens, None, None, None, C.byref(n), None))
@@ -461,6 +465,7 @@ def _indptr_host(kv_indptr) -> "C.Array":
 
 
 def decode_workspace_bytes(kv_indptr, n_req, Hq, Hkv, d, num_splits=0) -> int:
+    """Workspace size sta_decode_splitkv needs for these requests (host only)."""
     n = C.c_size_t(0)
     ind = _indptr_host(kv_indptr)
     _check("sta_decode_splitkv", lib().sta_decode_splitkv(None, None, None, None, ind, n_req, Hq, Hkv, d, STA_BF16,
@@ -562,6 +567,8 @@ def sta_merge_lse(part_o: torch.Tensor, part_lse: torch.Tensor, o_dtype=torch.bf
 
 
 def sta_device_error(reset: bool = True) -> int:
+    """The device error word (nonzero: a kernel's bounded wait gave up, or a damaged input was
+    met); synchronises, and clears the word when reset."""
     code = C.c_int(0)
     _check("sta_device_error", lib().sta_device_error(C.byref(code), int(reset)))
     return int(code.value)
