@@ -515,3 +515,56 @@ def test_mla_decode_single_token_and_constant_latent():
     kv2[:, :512] = kv[0, :512]
     o, _ = oracle.mla_decode(q, kv2, np.array([0, 4, 9]), scale=0.05)
     assert np.abs(o - kv[0, :512]).max() < 1e-12
+
+
+# ---- valid-element count of one mask head (the FLOP count of the reference arm)
+
+
+def test_mask_count_matches_hand_counts_and_closed_forms():
+    # hand-derived goldens: causal L=128 and the band |i-j| <= 64 at L=512
+    g = _read_golden("causal_L128_encoding.txt")
+    assert oracle.mask_count(W.pattern(causal=True), 128, 128) == g["n_valid"][0] == 128 * 129 // 2
+    g = _read_golden("band_L512_w64_counts.txt")
+    assert oracle.mask_count(W.pattern(win_lo=-64, win_hi=64), 512, 512) == g["n_valid"][0]
+    # closed forms: an unrestricted mask counts every element; an empty window none; the diagonal L
+    assert oracle.mask_count(W.pattern(), 37, 91) == 37 * 91
+    assert oracle.mask_count(W.pattern(win_lo=1, win_hi=0), 50, 50) == 0
+    assert oracle.mask_count(W.pattern(win_lo=0, win_hi=0), 77, 77) == 77
+    # causal with Lq < Lk: row i has i + 1 keys
+    assert oracle.mask_count(W.pattern(causal=True), 10, 300) == 55
+    # window of width w above the diagonal, clipped at the right edge: sum_i min(w + 1, L - i)
+    L, w = 100, 7
+    assert oracle.mask_count(W.pattern(win_lo=0, win_hi=w), L, L) == sum(min(w + 1, L - i) for i in range(L))
+
+
+@pytest.mark.parametrize("Lq,Lk,density", [(1, 1, 1.0), (33, 130, 0.3), (64, 64, 0.0), (200, 77, 0.05)])
+def test_mask_count_of_dense_masks_is_the_numpy_sum(Lq, Lk, density):
+    u8 = W.random_mask_u8(11, 7, Lq, Lk, density)
+    want = int(u8.astype(np.int64).sum())
+    assert oracle.mask_count(W.MaskHead("u8", data=u8), Lq, Lk) == want
+    # bit-packed: the same count, from numpy's own unpacking of the words
+    bits = W.pack_bits(u8)
+    unpacked = np.unpackbits(bits.view(np.uint8).reshape(Lq, -1), axis=1, bitorder="little")[:, :Lk]
+    assert oracle.mask_count(W.MaskHead("bits", data=bits), Lq, Lk) == int(unpacked.sum()) == want
+    # and the encoder's valid count (popcount of part tiles + 4096 per full tile) agrees
+    assert oracle.encode_mask([W.MaskHead("u8", data=u8)], Lq, Lk)["n_valid"] == want
+
+
+@pytest.mark.slow
+def test_mask_count_longformer_closed_form():
+    # causal and (i - j < 256 or j < 16) at L = 16384: 4,419,592 valid (closed form above)
+    assert oracle.mask_count(W.pattern(causal=True, win_lo=-255, n_global_cols=16), 16384, 16384) == 4419592
+
+
+def test_mask_count_bigbird_head_is_full_blocks_plus_random_bits():
+    # one BigBird head: 313 all-ones blocks of 4096, plus the kept elements of its random blocks
+    L = 4096
+    bits = W.bigbird_mask_bits(0, 1, L)[0]
+    full, rand = W.bigbird_blocks(0, 1, L)
+    kept = 0
+    u8 = np.unpackbits(bits.view(np.uint8).reshape(L, -1), axis=1, bitorder="little")[:, :L]
+    for qb in range(L // 64):
+        for c in rand[0][qb]:
+            kept += int(u8[qb * 64:(qb + 1) * 64, c * 64:(c + 1) * 64].sum())
+    assert sum(len(x) for x in full[0]) == 313
+    assert oracle.mask_count(W.MaskHead("bits", data=bits), L, L) == 313 * 4096 + kept
