@@ -391,9 +391,14 @@ sta_status sta_decode_splitkv_paged(const void* q, const void* k_pages, const vo
  * workspace: the caller still passes q, k, v, kv_indptr, o and lse. The partial
  * results go to one fixed 16 MiB array in the library's own device memory, which
  * every GPU that loads the library holds until the process exits. The plan must
- * fit it: slots * Hq * (d + 1) * 4 bytes (each part rounded up to 256) <= 16 MiB,
- * where slots = resident CTAs + n_req when num_splits == 0 and n_req * num_splits
- * otherwise; a larger plan returns STA_ERR_WORKSPACE and launches nothing.
+ * fit it: slots * Hq * (d + 1) * 4 bytes (each part rounded up to 256) <= 16 MiB.
+ * With num_splits > 0, slots = n_req * num_splits. With num_splits == 0, slots =
+ * ranges + n_req, where ranges (the token ranges the plan cuts the KV stream
+ * into) is at most ceil(T / 8) and at most the resident decode CTAs divided by
+ * the KV-head groups a CTA serves; the sum resident CTAs + n_req is therefore an
+ * upper bound, not the exact size. Query the exact size with sta_decode_splitkv
+ * (workspace == NULL). A larger plan returns STA_ERR_WORKSPACE and launches
+ * nothing.
  * The first call on each device looks up the array's device address (with that
  * device current); make that first call before any stream capture. All calls
  * share the array and it keeps the last call's contents (nothing in it needs
@@ -430,6 +435,17 @@ const char* sta_last_cuda_error_string(void);
  * instead of hanging; 0 means no such event. Copies the word to *code
  * (synchronous) and clears it when reset != 0. */
 sta_status sta_device_error(int* code, int reset);
+
+/* sta_check_bounded_wait -- exercises the failure-detection path on the GPU
+ * without a fault: one kernel waits, through the bounded mbarrier wait every
+ * kernel of this library uses, on a barrier phase that nothing completes. After
+ * limit_ns nanoseconds (1e3 <= limit_ns <= 2e9) the wait gives up, records code
+ * 0x7f1 in the device error word (read it with sta_device_error) unless an
+ * earlier code is there, writes 0 to *outcome_dev (int, device, 4-byte aligned;
+ * 1 would mean the wait completed) and the kernel returns: the context stays
+ * usable. (The pages have no counterpart: this checks the library's own
+ * hang-avoidance, not the method.) Asynchronous on `stream`. */
+sta_status sta_check_bounded_wait(int64_t limit_ns, int* outcome_dev, sta_stream stream);
 
 #ifdef __cplusplus
 }

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "internal.h"
 
@@ -17,9 +18,12 @@ static std::atomic<int> g_last_cuda_error{0};
 void note_cuda_error(cudaError_t e) { g_last_cuda_error.store((int)e); }
 
 int* device_error_word() {
+  // one lookup per device, cached; the lock keeps first calls from several host threads apart
+  static std::mutex mu;
   static int* cached[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!cached[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
