@@ -40,7 +40,7 @@ _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNE
 EXPORTED = ("sta_encode_mask", "sta_tile_lists_bytes", "sta_mha_fwd", "sta_mha_fwd_splitkv", "sta_mha_fwd_layout",
             "sta_bias_residual_layernorm", "sta_validate_mask", "sta_mla_decode", "sta_mha_select_kernel", "sta_decode_splitkv",
             "sta_decode_splitkv_noalloc", "sta_decode_splitkv_paged", "sta_merge_lse", "sta_status_string", "sta_device_error",
-            "sta_last_cuda_error", "sta_last_cuda_error_string")
+            "sta_check_bounded_wait", "sta_last_cuda_error", "sta_last_cuda_error_string")
 
 BIG = 1 << 40
 
@@ -101,6 +101,7 @@ def lib():
             h.sta_status_string.argtypes = [i32]
             h.sta_status_string.restype = C.c_char_p
             h.sta_device_error.argtypes = [C.POINTER(C.c_int), i32]
+            h.sta_check_bounded_wait.argtypes = [C.c_int64, P, P]
             h.sta_last_cuda_error.argtypes = []
             h.sta_last_cuda_error_string.argtypes = []
             h.sta_last_cuda_error_string.restype = C.c_char_p
@@ -564,6 +565,15 @@ def sta_merge_lse(part_o: torch.Tensor, part_lse: torch.Tensor, o_dtype=torch.bf
     _check("sta_merge_lse", lib().sta_merge_lse(_ptr(part_o.contiguous()), _ptr(part_lse.contiguous()), n_rows, s, d,
                                                 _ptr(o), _dtype_code(o.dtype), _ptr(lse), _stream(stream)))
     return o, lse
+
+
+def sta_check_bounded_wait(limit_ns: int, stream=None) -> int:
+    """Run the failure-detection check (a bounded wait on a barrier nothing completes, limit
+    limit_ns); returns the kernel's outcome (0: the wait gave up, as it must). The device
+    error word then holds 0x7f1 unless an earlier code is there."""
+    out = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check("sta_check_bounded_wait", lib().sta_check_bounded_wait(int(limit_ns), _ptr(out), _stream(stream)))
+    return int(out.item())
 
 
 def sta_device_error(reset: bool = True) -> int:

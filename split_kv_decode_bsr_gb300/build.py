@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsta.so")
-SOURCES = ["api.cu", "encode.cu", "mha_row.cu", "mha_block.cu", "decode.cu", "decode_noalloc.cu", "epilogue.cu", "validate.cu", "mla.cu"]
+SOURCES = ["api.cu", "encode.cu", "mha_row.cu", "mha_block.cu", "decode.cu", "decode_noalloc.cu", "epilogue.cu", "validate.cu", "mla.cu", "diag.cu"]
 HEADERS = ["common.cuh", "internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

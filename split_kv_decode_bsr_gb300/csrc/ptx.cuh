@@ -66,13 +66,16 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 }
 constexpr uint32_t kSuspendHintNs = 1000000u;  // 1 ms per try: the time limit is checked between tries
 
-// Wait for the phase with the given parity to complete; false after the time limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int err_code) {
+// Wait for the phase with the given parity to complete; false after `limit_ns` (the
+// kernels use kWaitLimitNs; a shorter limit serves the failure-detection check).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int err_code,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
+  const uint32_t hint = limit_ns < kSuspendHintNs ? (uint32_t)limit_ns : kSuspendHintNs;
   for (;;) {
-    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_error(err, err_code);
       return false;
     }

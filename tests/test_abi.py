@@ -260,3 +260,10 @@ def test_mla_decode_host_checks(lib):
     assert call(indptr=bad) == sta.STA_ERR_INVALID_ARG
     bad0 = (C.c_int32 * 4)(3, 100, 100, 5000)  # not starting at 0
     assert call(indptr=bad0) == sta.STA_ERR_INVALID_ARG
+
+
+def test_bounded_wait_check_rejects_bad_limits_on_the_host(lib):
+    # limits outside [1 us, 2 s] and a missing outcome pointer launch nothing
+    for limit, out in ((999, 16), (2_000_000_001, 16), (-5, 16), (1_000_000, None)):
+        assert lib.sta_check_bounded_wait(limit, out, None) == sta.STA_ERR_INVALID_ARG
+    assert lib.sta_check_bounded_wait(1_000_000, 18, None) == sta.STA_ERR_UNSUPPORTED  # misaligned
