@@ -2,14 +2,16 @@
 """Benchmark of the masked-MHA / split-KV decode path on GB300.
 
 One JSON line on rank 0. Headline: valid-pair TFLOP/s of the masked MHA forward
-(4*d FLOPs per unmasked (q, k) pair per head) on the BERT-base-shaped band-64
-workload (B=8, H=12, L=512, d=64, bf16). The same line carries the split-KV GQA
-decode (KV-read GB/s) and the BigBird and Longformer workloads as secondary
-objects, each with its roofline fraction against the measured GB300 peaks.
+(4*d FLOPs per unmasked (q, k) pair per head) on the largest configured workload,
+the Longformer-style mask with one random head (B=1, H=32, L=16384, d=128, bf16),
+with its roofline against the measured GB300 peaks. The same line carries the
+other configured workloads (BERT band, BigBird, the split-KV GQA decode in
+KV-read GB/s) and the widening rows as secondary objects under "workloads", and
+ends with a compact "summary" of every figure (value, unit, roofline fraction,
+ms), so that a reader of the line's tail sees all of them.
 
-A step is one sta_mha_fwd_splitkv call with the library's split plan (the
-block kernel, plus the log-sum-exp merge when a head is split; mask encoded
-once, outside the timed region).
+A step is one sta_mha_fwd_splitkv call with the library's split plan and kernel
+choice (mask encoded once, outside the timed region).
 L2 is flushed (a 256 MiB write, then a read of another 256 MiB buffer so that
 no dirty line of the flush is left to write back, outside the CUDA events)
 before every timed launch. The device time is the sum of per-launch CUDA-event durations on the
@@ -397,6 +399,8 @@ class MlaBench:
         self.step()
         self.ho.copy_(self.o, non_blocking=True)
 
+    kernel_desc = "mma.sync m16n8k16 bf16 (16 query heads as M)"
+
     def launches_per_step(self):
         return 2  # decode (+ the merge of the requests cut into chunks)
 
@@ -540,15 +544,26 @@ def cpu_baseline(wl, flops, target_s):
 # ---------------------------------------------------------------------------
 
 
+L2_NOTE = ("inputs of the configured workloads exceed or approach the 129 MB L2; the GPU arm flushes L2 before "
+           "every timed launch (256 MiB write, then a 256 MiB read)")
+
+
+def mha_config(wl, pairs, world):
+    """The workload description both arms report (identical dicts, so the two lines compare)."""
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "L": wl.Lq, "d": wl.d, "mask": wl.meta.get("mask", ""),
+            "valid_pairs": int(pairs), "l2": L2_NOTE, "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, dist):
-    """Reference arm: the CPU oracle, as it stands, on the headline workload."""
+    """Reference arm: the CPU oracle, as it stands, on the headline workload (one full pass per step)."""
     if dist.rank != 0:
         return
     wl = mha_workload(args.workload)
     import oracle
 
     heads_valid = [oracle.mask_count(m, wl.Lq, wl.Lk) for m in wl.mask_heads]
-    flops = 4.0 * wl.d * valid_pairs(wl, heads_valid)
+    pairs = valid_pairs(wl, heads_valid)
+    flops = 4.0 * wl.d * pairs
     for _ in range(args.warmup):
         oracle_mha_seconds(wl)
     times = [oracle_mha_seconds(wl) for _ in range(args.steps)]
@@ -557,7 +572,7 @@ def run_reference(args, dist):
     line = {"impl": "reference", "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "L": wl.Lq, "d": wl.d},
+            "config": mha_config(wl, pairs, args.gpus),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"full {wl.name} workload per step, fp64 C oracle"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -584,17 +599,48 @@ def mha_roofline(b, t, peaks, traffic, which):
     return r
 
 
+def summary_entry(d):
+    """value, unit, roofline fraction (with its bound) and ms of one workload object."""
+    r = d.get("roofline") or {}
+    e = {"value": round(d["value"], 4), "unit": d["unit"], "ms": round(d["ms_per_step"], 5)}
+    if r:
+        e["frac"] = round(r["frac"], 4)
+        e["bound"] = r["bound"]
+    return e
+
+
+def measure_mha(name, dev, args, dist, flush, peaks, peak_src, steps):
+    """One masked-MHA workload through sta_mha_fwd_splitkv (library plan): timing, roofline."""
+    b = MhaBench(name, dev, args.mha_splits)
+    g = graphed(b.step)
+    ms, wall = time_device(g, steps, args.warmup, dist, flush)
+    t = sum(ms) / len(ms) / 1e3
+    kf = "mha_block.cu" if b.kernel == "block" else "mha_row.cu"
+    out = {
+        "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": b.flops / t / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": 1e3 * t, "config": mha_config(b.wl, b.pairs, dist.world),
+        "launch": {"kernel": b.kernel, "split_kv": "planned" if b.split else "none", "workspace_bytes": b.ws.numel()},
+        "tensor_frac": (b.flops / t / 1e12) / peaks["bf16_tflops"],
+        "roofline": mha_roofline(b, t, peaks, recorded_traffic(kf, name), peak_src),
+        "gpu_launches": b.launches_per_step() * steps,
+        "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
+    }
+    return b, out, ms, wall
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="sta", choices=["sta", "reference"])
-    ap.add_argument("--workload", default="bert-band")
-    ap.add_argument("--extra", default="bigbird,longformer,decode,decode-paged,long-causal,causal-1head,sparse-random,"
-                                       "epilogue-ln,mha-token-major,mla-decode",
-                    help="comma list of secondary workloads (bigbird, longformer, decode, decode-paged, long-causal, "
-                         "causal-1head, sparse-random, epilogue-ln, mha-token-major, mla-decode) or 'none'")
+    ap.add_argument("--workload", default="longformer",
+                    help="headline masked-MHA workload (default: the Longformer + random head, the largest)")
+    ap.add_argument("--extra", default="bert-band,bigbird,decode,decode-paged,long-causal,causal-1head,"
+                                       "sparse-random,epilogue-ln,mha-token-major,mla-decode",
+                    help="comma list of secondary workloads (bert-band, bigbird, longformer, decode, decode-paged, "
+                         "long-causal, causal-1head, sparse-random, epilogue-ln, mha-token-major, mla-decode) or "
+                         "'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")
@@ -627,55 +673,43 @@ def main():
         flush_buf.fill_(1)
         clean_buf.sum()
 
-    # ---- headline: masked MHA on the BERT-base band workload
-    mb = MhaBench(args.workload, dev, args.mha_splits)
+    # ---- headline: masked MHA on the largest configured workload
     with ClockSampler(dist.local) as clk:
-        g_mb = graphed(mb.step)
-        ms, wall = time_device(g_mb, args.steps, args.warmup, dist, flush)
-    stats = timing_stats(ms, g_mb, args.steps, args.warmup, dist)
+        mb, head, ms, wall = measure_mha(args.workload, dev, args, dist, flush, peaks, peak_src, args.steps)
     dev_s = dist.max(sum(ms) / 1e3)
     total_flops = dist.sum(mb.flops * args.steps)
     value = total_flops / dev_s / 1e12
     ms_per_step = 1e3 * dev_s / args.steps
-    kernel_ms = None
     if args.sweep_kernels:
-        kernel_ms = {k: sum(time_device(graphed(lambda: mb.step(k)), args.steps, args.warmup, dist, flush)[0]) /
-                        args.steps
-                     for k in ("block", "row")}
+        head["launch"]["kernel_ms"] = {
+            k: sum(time_device(graphed(lambda: mb.step(k)), args.steps, args.warmup, dist, flush)[0]) / args.steps
+            for k in ("block", "row")}
     e2e_s = time_e2e(mb.step_e2e, args.steps, args.warmup, dist)
     e2e_value = total_flops / e2e_s / 1e12
-    kfile = "mha_block.cu" if mb.kernel == "block" else "mha_row.cu"
-    avg_launch_s = sum(ms) / len(ms) / 1e3
-    achieved = mb.bytes / avg_launch_s / 1e9
     line = {
         "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": value, "unit": "TFLOP/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": mb.wl.name, "B": mb.wl.B, "H": mb.wl.H, "L": mb.wl.Lq, "d": mb.wl.d,
-                   "mask": "sliding window |i-j|<=64", "valid_pairs": mb.pairs, "kernel": mb.kernel,
-                   "split_kv": "planned" if mb.split else "none",
-                   "l2": "flushed before every timed launch (256 MiB write, then a 256 MiB read)", "parallelism": f"replicas x{dist.world}",
-                   "timing": "CUDA events around a CUDA-graph replay of one library call per step"},
-        "tensor_frac": (mb.flops / avg_launch_s / 1e12) / peaks["bf16_tflops"],
-        "roofline": roofline_obj("hbm", achieved, peaks["hbm_gbs"], "GB/s", recorded_traffic(kfile, mb.name),
-                                 peak_src),
+        "config": head["config"],
+        "launch": dict(head["launch"], timing="CUDA events around a CUDA-graph replay of one library call per step"),
+        "tensor_frac": head["tensor_frac"],
+        "roofline": head["roofline"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": mb.h2d_bytes,
                 "d2h_bytes_per_step": mb.d2h_bytes},
-        "gpu_launches": mb.launches_per_step() * args.steps,
+        "gpu_launches": head["gpu_launches"],
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
-        "timing_stats": stats,
+        "timing_stats": head["timing_stats"],
     }
-    line["roofline"]["algorithmic_bytes_per_launch"] = mb.bytes
-    if kernel_ms:
-        line["config"]["kernel_ms"] = kernel_ms
-    if dist.rank == 0 and dist.world >= 1:
+    if dist.rank == 0:
         line["cpu_baseline"] = cpu_baseline(mb.wl, mb.flops, args.cpu_seconds) if dist.world == 1 else None
     del mb
+    torch.cuda.empty_cache()
+    summary = {args.workload: summary_entry(dict(head, ms_per_step=ms_per_step, value=value))}
 
     # ---- secondary workloads
     extras = {}
-    wanted = [] if args.extra == "none" else [x for x in args.extra.split(",") if x]
+    wanted = [] if args.extra == "none" else [x for x in args.extra.split(",") if x and x != args.workload]
     for name in wanted:
         steps = max(3, min(args.steps, 10))
         if name == "epilogue-ln":
@@ -699,8 +733,7 @@ def main():
                 "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
             }
             del eb
-            continue
-        if name == "mla-decode":
+        elif name == "mla-decode":
             mb2 = MlaBench(dev)
             g = graphed(mb2.step)
             ms, _ = time_device(g, steps, args.warmup, dist, flush)
@@ -710,7 +743,7 @@ def main():
                 "metric": "MLA decode KV-read GB/s", "value": mb2.kv_bytes / t / 1e9, "unit": "GB/s",
                 "ms_per_step": 1e3 * t, "tflops": mb2.flops / t / 1e12,
                 "config": {"workload": mb2.wl.name, "T": mb2.T, "kv_bytes": mb2.kv_bytes, "chunking": "library",
-                           "kernel": "mma.sync m16n8k16 bf16 (16 query heads as M)"},
+                           "kernel": mb2.kernel_desc},
                 "roofline": roofline_obj("hbm", mb2.bytes / t / 1e9, peaks["hbm_gbs"], "GB/s",
                                          recorded_traffic("mla.cu", name), peak_src),
                 "e2e": {"value": mb2.kv_bytes / (e2e_s / steps) / 1e9, "unit": "GB/s",
@@ -719,8 +752,7 @@ def main():
                 "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
             }
             del mb2
-            continue
-        if name == "mha-token-major":
+        elif name == "mha-token-major":
             b = MhaBench("longformer", dev, args.mha_splits)
             ob = torch.empty((b.wl.B, b.wl.Lq, b.wl.H, b.wl.d), dtype=b.q.dtype, device=dev)
 
@@ -745,8 +777,7 @@ def main():
                 "gpu_launches": b.launches_per_step() * steps,
             }
             del b, ob
-            continue
-        if name in ("decode", "decode-paged"):
+        elif name in ("decode", "decode-paged"):
             db = DecodeBench(dev, 16 if name == "decode-paged" else 0)
             g = graphed(db.step)
             ms, _ = time_device(g, steps, args.warmup, dist, flush)
@@ -768,21 +799,7 @@ def main():
             }
             del db
         else:
-            b = MhaBench(name, dev, args.mha_splits)
-            g = graphed(b.step)
-            ms, _ = time_device(g, steps, args.warmup, dist, flush)
-            t = sum(ms) / len(ms) / 1e3
-            tf = b.flops / t / 1e12
-            kf = "mha_block.cu" if b.kernel == "block" else "mha_row.cu"
-            extras[name] = {
-                "metric": "valid-pair TFLOP/s (masked MHA fwd)", "value": tf, "unit": "TFLOP/s", "ms_per_step": 1e3 * t,
-                "config": {"workload": b.wl.name, "valid_pairs": b.pairs, "kernel": b.kernel,
-                           "split_kv": "planned" if b.split else "none", "workspace_bytes": b.ws.numel()},
-                "tensor_frac": tf / peaks["bf16_tflops"],
-                "roofline": mha_roofline(b, t, peaks, recorded_traffic(kf, name), peak_src),
-                "gpu_launches": b.launches_per_step() * steps,
-                "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
-            }
+            b, extras[name], _, _ = measure_mha(name, dev, args, dist, flush, peaks, peak_src, steps)
             if b.encode_input_bytes:  # the encoder, timed apart: the fill call over the dense mask input
                 ms_e, _ = time_device(graphed(b.mask.refill), steps, args.warmup, dist, flush)
                 te = sum(ms_e) / len(ms_e) / 1e3
@@ -795,15 +812,18 @@ def main():
                 extras[name]["unsplit_ms"] = sum(ms1) / len(ms1)
                 del nb
             if args.sweep_kernels:
-                extras[name]["kernel_ms"] = {
+                extras[name]["launch"]["kernel_ms"] = {
                     k: sum(time_device(graphed(lambda: b.step(k)), steps, args.warmup, dist, flush)[0]) / steps
                     for k in ("block", "row")}
             del b
+        summary[name] = summary_entry(extras[name])
         torch.cuda.empty_cache()
     line["workloads"] = extras
     err = sta.sta_device_error()
     if err:
         line["device_error"] = err
+    # last key: one short entry per workload, so the end of the line holds every figure
+    line["summary"] = summary
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()

@@ -20,7 +20,7 @@ def test_reference_arm_two_ranks():
     env = dict(os.environ, STA_BENCH_BACKEND="gloo", CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
            "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference", "--gpus", "2",
-           "--steps", "1", "--warmup", "3"]
+           "--steps", "1", "--warmup", "3", "--workload", "bert-band"]
     out = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [json.loads(x) for x in out.stdout.splitlines() if x.startswith("{")]
@@ -31,3 +31,8 @@ def test_reference_arm_two_ranks():
         assert key in d, key
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # the same workload description the GPU arm reports (61,888 valid pairs per head, 96 heads)
+    import bench
+    import workloads as W
+
+    assert d["config"] == bench.mha_config(W.bert_band(), 96 * 61888, 2)

@@ -283,14 +283,15 @@ def tiny_causal(seed: int = 0) -> MhaWorkload:
     B, H, L, d = 1, 2, 128, 64
     q, k, v = _qkv(seed, B, H, L, L, d, "f32")
     return MhaWorkload("tiny-causal-fp32 B1 H2 L128 d64", B, H, L, L, d, "f32", q, k, v,
-                       [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d))
+                       [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d), {"mask": "causal j <= i"})
 
 
 def bert_band(seed: int = 0, B: int = 8, H: int = 12, L: int = 512, d: int = 64, w: int = 64) -> MhaWorkload:
     """BERT-base-shaped sliding window |i - j| <= w, bf16."""
     q, k, v = _qkv(seed, B, H, L, L, d, "bf16")
     return MhaWorkload(f"bert-band{w} bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
-                       [pattern(win_lo=-w, win_hi=w)], [0] * H, 1.0 / math.sqrt(d))
+                       [pattern(win_lo=-w, win_hi=w)], [0] * H, 1.0 / math.sqrt(d),
+                       {"mask": f"sliding window |i-j| <= {w}"})
 
 
 def long_causal(seed: int = 0, B: int = 1, H: int = 2, L: int = 32768, d: int = 128) -> MhaWorkload:
@@ -299,7 +300,7 @@ def long_causal(seed: int = 0, B: int = 1, H: int = 2, L: int = 32768, d: int = 
     per SM evenly)."""
     q, k, v = _qkv(seed, B, H, L, L, d, "bf16", mult=0.5)
     return MhaWorkload(f"long-causal bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
-                       [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d))
+                       [pattern(causal=True)], [0] * H, 1.0 / math.sqrt(d), {"mask": "causal j <= i"})
 
 
 def sparse_random(seed: int = 0, B: int = 1, H: int = 8, L: int = 4096, d: int = 64,
@@ -310,7 +311,8 @@ def sparse_random(seed: int = 0, B: int = 1, H: int = 8, L: int = 4096, d: int =
     q, k, v = _qkv(seed, B, H, L, L, d, "bf16")
     rnd = MaskHead("bits", data=random_mask_bits(seed, STREAM_MASK_ELEMS, L, L, density))
     return MhaWorkload(f"sparse-random{density:g} bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
-                       [rnd], [0] * H, 1.0 / math.sqrt(d))
+                       [rnd], [0] * H, 1.0 / math.sqrt(d),
+                       {"mask": f"i.i.d. Bernoulli({density:g}) per element, one mask head for all heads"})
 
 
 def bigbird_blocks(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3):
@@ -380,7 +382,9 @@ def bigbird(seed: int = 0, B: int = 4, H: int = 16, L: int = 4096, d: int = 64) 
     bits = bigbird_mask_bits(seed, H, L)
     heads = [MaskHead("bits", data=bits[h]) for h in range(H)]
     return MhaWorkload(f"bigbird bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
-                       heads, list(range(H)), 1.0 / math.sqrt(d))
+                       heads, list(range(H)), 1.0 / math.sqrt(d),
+                       {"mask": "64x64 blocks per query block: 3 window, 2 global, 3 random (elements kept "
+                                "with p=0.5); one mask head per attention head"})
 
 
 def longformer(seed: int = 0, B: int = 1, H: int = 32, L: int = 16384, d: int = 128,
@@ -397,7 +401,9 @@ def longformer(seed: int = 0, B: int = 1, H: int = 32, L: int = 16384, d: int = 
     rnd = MaskHead("bits", data=random_mask_bits(seed, STREAM_MASK_ELEMS, L, L, density))
     head_map = [0] * (H - 1) + [1]
     return MhaWorkload(f"longformer+random bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
-                       [structured, rnd], head_map, 1.0 / math.sqrt(d))
+                       [structured, rnd], head_map, 1.0 / math.sqrt(d),
+                       {"mask": f"heads 0..{H - 2}: causal and (i-j < {window} or j < {n_global}); head {H - 1}: "
+                                f"i.i.d. Bernoulli({density:g}) per element"})
 
 
 @dataclass
