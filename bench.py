@@ -233,7 +233,8 @@ def mha_workload(name):
 
     return {"bert-band": W.bert_band, "bigbird": W.bigbird, "longformer": W.longformer,
             "tiny-causal": W.tiny_causal, "long-causal": W.long_causal,
-            "causal-1head": lambda: W.long_causal(H=1, L=16384), "sparse-random": W.sparse_random}[name]()
+            "causal-1head": lambda: W.long_causal(H=1, L=16384), "sparse-random": W.sparse_random,
+            "mixed-sparse": W.mixed_sparse}[name]()
 
 
 def algorithmic_bytes_mha(wl, mask):
@@ -278,7 +279,7 @@ class MhaBench:
         self.num_splits = num_splits
         ws = sta.mha_splitkv_workspace_bytes(self.mask, wl.B, wl.H, wl.d, self.q.dtype, head_map=wl.head_map,
                                              num_splits=num_splits)
-        self.split = self.kernel == "block" and ws > 256
+        self.split = self.kernel in ("block", "mixed") and ws > 256
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.hq, self.hk, self.hv = (x.cpu().pin_memory() for x in (self.q, self.k, self.v))
         self.ho = torch.empty_like(self.o, device="cpu").pin_memory()
@@ -310,7 +311,8 @@ class MhaBench:
         return sum(x.numel() * x.element_size() for x in (self.ho, self.hlse))
 
     def launches_per_step(self):
-        return 2 if self.split else 1  # block kernel (+ the merge of split heads)
+        # block or row kernel, or both under the per-head choice (+ the merge of split heads)
+        return (2 if self.kernel == "mixed" else 1) + (1 if self.split else 0)
 
 
 class DecodeBench:
@@ -637,10 +639,10 @@ def main():
     ap.add_argument("--workload", default="longformer",
                     help="headline masked-MHA workload (default: the Longformer + random head, the largest)")
     ap.add_argument("--extra", default="bert-band,bigbird,decode,decode-paged,long-causal,causal-1head,"
-                                       "sparse-random,epilogue-ln,mha-token-major,mla-decode",
+                                       "sparse-random,mixed-sparse,epilogue-ln,mha-token-major,mla-decode",
                     help="comma list of secondary workloads (bert-band, bigbird, longformer, decode, decode-paged, "
-                         "long-causal, causal-1head, sparse-random, epilogue-ln, mha-token-major, mla-decode) or "
-                         "'none'")
+                         "long-causal, causal-1head, sparse-random, mixed-sparse, epilogue-ln, mha-token-major, "
+                         "mla-decode) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")
@@ -811,7 +813,7 @@ def main():
                 ms1, _ = time_device(graphed(nb.step), steps, args.warmup, dist, flush)
                 extras[name]["unsplit_ms"] = sum(ms1) / len(ms1)
                 del nb
-            if args.sweep_kernels:
+            if args.sweep_kernels or b.kernel == "mixed":  # each kernel alone on every head, for comparison
                 extras[name]["launch"]["kernel_ms"] = {
                     k: sum(time_device(graphed(lambda: b.step(k)), steps, args.warmup, dist, flush)[0]) / steps
                     for k in ("block", "row")}

@@ -118,11 +118,18 @@ typedef struct {
    *                                   tile (row 2t+1 beyond ot_rows is empty)
    * Only for ot_cols <= 1024 (the block-wise kernel's limit). */
   void* tile_lists;
+  /* Optional HOST array [Hm] (caller-owned) or NULL. When set, the size query
+   * of sta_encode_mask stores each mask head's number of valid elements there.
+   * With head_tiles and head_valid both set, STA_KERNEL_AUTO chooses the kernel
+   * per mask head (STOF カーネル選択 per head group) instead of once for the
+   * whole mask; results do not depend on it beyond rounding. */
+  int64_t* head_valid;
 } sta_bsr_mask;
 
 /* sta_validate_mask -- check a two-level mask whose arrays are HOST copies
  * (full_row_ptr, full_col_idx, part_row_ptr, part_col_idx, part_bitmap and, when
- * set, tile_lists all point to host memory; head_tiles is ignored). Returns
+ * set, tile_lists all point to host memory; head_tiles and head_valid are
+ * ignored). Returns
  * STA_OK when the mask is one that sta_encode_mask could have produced, else
  * STA_ERR_INVALID_ARG with *failed_check (may be NULL) set to the first failed
  * check:
@@ -221,6 +228,9 @@ sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, int Lk, sta
 #define STA_KERNEL_AUTO 0  /* analytic selector (STOF カーネル選択)           */
 #define STA_KERNEL_BLOCK 1 /* block-wise: TMA + tcgen05/TMEM, bf16 only        */
 #define STA_KERNEL_ROW 2   /* row-wise: one warp per query row, bf16 or f32   */
+#define STA_KERNEL_MIXED 3 /* returned by sta_mha_select_kernel only: the     *
+                            * per-head choice runs both kernels, each on its  *
+                            * own heads, concurrently                         */
 
 /* sta_mha_fwd -- O = softmax(Q K^T * scale + mask) V and its LSE, over the
  * valid elements of an encoded mask (STOF 問題定義, 統合 MHA モジュール).
@@ -239,7 +249,14 @@ sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, int Lk, sta
  *   dtype    STA_BF16 (both kernels) or STA_F32 (row-wise kernel only)
  *   scale    softmax scale, > 0 (e.g. 1/sqrt(d))
  *   kernel   STA_KERNEL_AUTO / BLOCK / ROW; BLOCK needs bf16 and Lk <= 65536
- *            (else STA_ERR_UNSUPPORTED)
+ *            (else STA_ERR_UNSUPPORTED). AUTO applies the analytic selector:
+ *            per mask head when mask->head_tiles and mask->head_valid are both
+ *            set, else once for the whole mask. When the per-head choice picks
+ *            both kernels, the row-wise kernel runs on its heads on a stream of
+ *            the library's own (created on the first such call on a device,
+ *            forked from and joined back into `stream` with events, so the call
+ *            stays asynchronous and can be captured in a CUDA graph) while the
+ *            block-wise kernel runs on the others on `stream`.
  * Pointers must be 16-byte aligned. Asynchronous on `stream`. */
 sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const sta_bsr_mask* mask,
                        const int32_t* head_map, int B, int H, int Lq, int Lk, int d, sta_dtype dtype, float scale,
@@ -319,8 +336,10 @@ sta_status sta_bias_residual_layernorm(const void* x, const void* bias, const vo
                                        sta_dtype dtype, sta_stream stream);
 
 /* Which kernel sta_mha_fwd would run for these arguments under
- * STA_KERNEL_AUTO (STA_KERNEL_BLOCK or STA_KERNEL_ROW), or a negative
- * sta_status on invalid arguments. Host only. */
+ * STA_KERNEL_AUTO: STA_KERNEL_BLOCK or STA_KERNEL_ROW, or STA_KERNEL_MIXED
+ * when the per-head choice (mask->head_tiles and mask->head_valid set) picks
+ * both kernels among the mask heads; a negative sta_status on invalid
+ * arguments. Host only. */
 int sta_mha_select_kernel(const sta_bsr_mask* mask, int B, int H, int Lq, int Lk, int d, sta_dtype dtype);
 
 /* ------------------------------------------------------------------------ */

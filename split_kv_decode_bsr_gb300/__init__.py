@@ -33,7 +33,7 @@ LIB_PATH = os.path.join(_HERE, "libsta.so")
 STA_OK, STA_ERR_INVALID_ARG, STA_ERR_UNSUPPORTED, STA_ERR_WORKSPACE, STA_ERR_CUDA = 0, 1, 2, 3, 4
 STA_BF16, STA_F32 = 0, 1
 STA_MASK_PATTERN, STA_MASK_DENSE_U8, STA_MASK_DENSE_BITS = 0, 1, 2
-STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW = 0, 1, 2
+STA_KERNEL_AUTO, STA_KERNEL_BLOCK, STA_KERNEL_ROW, STA_KERNEL_MIXED = 0, 1, 2, 3
 STA_O_BHLD, STA_O_BLHD = 0, 1
 _KERNELS = {"auto": STA_KERNEL_AUTO, "block": STA_KERNEL_BLOCK, "row": STA_KERNEL_ROW}
 
@@ -65,7 +65,7 @@ class _BsrMask(C.Structure):
                 ("ot_cols", C.c_int32), ("full_row_ptr", C.c_void_p), ("full_col_idx", C.c_void_p),
                 ("part_row_ptr", C.c_void_p), ("part_col_idx", C.c_void_p), ("part_bitmap", C.c_void_p),
                 ("n_full", C.c_int64), ("n_part", C.c_int64), ("n_valid", C.c_int64),
-                ("head_tiles", C.c_void_p), ("tile_lists", C.c_void_p)]
+                ("head_tiles", C.c_void_p), ("tile_lists", C.c_void_p), ("head_valid", C.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -186,6 +186,7 @@ class BsrMask:
         self.part_bitmap = part_bitmap
         self.n_full, self.n_part, self.n_valid = n_full, n_part, n_valid
         self.head_tiles = None  # ctypes int64 array [Hm] when known
+        self.head_valid = None  # ctypes int64 array [Hm] when known (with head_tiles: per-head kernel choice)
         self.tile_lists = None  # uint8 device tensor of the block kernel's column lists, when encoded
 
     def struct(self) -> _BsrMask:
@@ -199,6 +200,7 @@ class BsrMask:
         s.n_full, s.n_part, s.n_valid = self.n_full, self.n_part, self.n_valid
         s.head_tiles = C.cast(self.head_tiles, C.c_void_p) if self.head_tiles is not None else None
         s.tile_lists = self.tile_lists.data_ptr() if self.tile_lists is not None else None
+        s.head_valid = C.cast(self.head_valid, C.c_void_p) if self.head_valid is not None else None
         return s
 
     def refill(self, stream=None):
@@ -283,6 +285,8 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
     out.full_row_ptr, out.part_row_ptr = frp.data_ptr(), prp.data_ptr()
     head_tiles = (C.c_int64 * Hm)()
     out.head_tiles = C.cast(head_tiles, C.c_void_p)
+    head_valid = (C.c_int64 * Hm)()
+    out.head_valid = C.cast(head_valid, C.c_void_p)
     st = _stream(stream)
     _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
     nf, npart, nv = int(out.n_full), int(out.n_part), int(out.n_valid)
@@ -296,6 +300,7 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
     _check("sta_encode_mask", h.sta_encode_mask(arr, Hm, Lq, Lk, C.byref(out), _ptr(ws), C.byref(ws_bytes), st))
     m = BsrMask(Hm, Lq, Lk, frp, fci[:nf], prp, pci[:npart], pbm[:npart * 64], nf, npart, nv)
     m.head_tiles = head_tiles
+    m.head_valid = head_valid
     m.tile_lists = tl
     m._fill = (arr, out, ws, ws_bytes, srcs)  # keeps the sources alive for refill()
     return m
@@ -306,12 +311,13 @@ def sta_encode_mask(srcs: Sequence[MaskSource], Lq: int, Lk: int, device=None, s
 
 
 def sta_mha_select_kernel(mask: BsrMask, B: int, H: int, d: int, dtype=torch.bfloat16) -> str:
-    """Which kernel sta_mha_fwd would run under kernel="auto": "block" or "row" (host only)."""
+    """Which kernel sta_mha_fwd would run under kernel="auto": "block", "row", or "mixed" when the
+    per-mask-head choice (mask.head_tiles and mask.head_valid known) picks both (host only)."""
     s = mask.struct()
     r = lib().sta_mha_select_kernel(C.byref(s), B, H, mask.Lq, mask.Lk, d, _dtype_code(dtype))
     if r < 0:
         raise StaError("sta_mha_select_kernel", -r)
-    return {STA_KERNEL_BLOCK: "block", STA_KERNEL_ROW: "row"}[r]
+    return {STA_KERNEL_BLOCK: "block", STA_KERNEL_ROW: "row", STA_KERNEL_MIXED: "mixed"}[r]
 
 
 def sta_mha_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: BsrMask, head_map=None, scale=None,

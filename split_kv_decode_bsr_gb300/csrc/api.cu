@@ -37,27 +37,42 @@ namespace {
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Analytic selector (STOF カーネル選択: mask sparsity and sequence length decide
-// between the row-wise and the block-wise kernel). Cost model, per query head:
-//   block: every non-empty outer tile costs a 128x64 tile pair of MMAs plus the
-//          softmax of 64x64 scores;   t_b = (n_full + n_part) * 4096 * kBlockPair
-//   row:   every valid (q, k) pair costs FMA-pipe work, a K and a V row load and a
-//          warp reduction;             t_r = n_valid * d * kRowPair
-// The ratio of the constants comes from GB300 measurements at d = 64 (bench.py
-// --sweep-kernels): on an unstructured mask of 0.4 % density (B=1, H=8, L=4096) the
-// two kernels take 77 us (row) and 82 us (block), i.e. the row kernel spends ~230x
-// the block kernel's time per computed pair on each valid pair, so it wins only below
-// ~0.4 % valid density inside the non-empty tiles; on the BERT band (47 % inside the
-// computed tiles) it takes 312 us against 21 us.
-constexpr double kBlockPairPerD = 1.0 / 64.0;   // relative cost of one computed pair per unit d (block)
-constexpr double kRowPairPerD = 230.0 / 64.0;   // relative cost of one valid pair per unit d (row)
+// between the row-wise and the block-wise kernel), per mask head when the mask carries
+// per-head counts. Cost model:
+//   block: every non-empty outer tile costs a 128x64 tile pair of MMAs and the softmax of
+//          64x64 scores, whatever its fill:      t_b = tiles * 4096
+//   row:   every valid (q, k) pair costs two row loads, FMA-pipe work and its share of a
+//          batched warp reduction:               t_r = valid * kRowOverBlock(d)
+// The ratio is the measured crossover on GB300. Unstructured masks over B=1, H=8, L=4096
+// (every outer tile part; time in us, row / block):
+//   density   0.1 %      0.2 %      0.4 %      1 %         2 %         5 %
+//   d = 64    55 / 82    64 / 82    80 / 82    125 / 82    186 / 81    326 / 81
+//   d = 128   58 / 80    68 / 80    91 / 80    152 / 80    239 / 80    447 / 80
+// The block kernel's time does not follow the fill of its tiles (part tiles are bound by
+// the softmax at both head sizes), the row kernel's follows the valid pairs; the two meet
+// near 0.45 % density at d = 64 and 0.3 % at d = 128, i.e. the row kernel spends ~220x
+// (d = 64) and ~330x (d = 128) the block kernel's time per computed pair on each valid pair.
+double row_over_block(int d) { return d == 64 ? 220.0 : 330.0; }
 constexpr int kMaxSplitsPrefill = 1024;
 
+int choose(int64_t tiles, int64_t valid, int d) {
+  const double t_block = (double)tiles * 4096.0;
+  const double t_row = (double)valid * row_over_block(d);
+  return t_row < t_block ? STA_KERNEL_ROW : STA_KERNEL_BLOCK;
+}
+
+// The choice for the whole mask (from its total counts).
 int select_kernel(const sta_bsr_mask* m, int d, int Lk, sta_dtype dtype) {
   if (dtype != STA_BF16 || !block_kernel_supports(d, Lk, dtype)) return STA_KERNEL_ROW;
-  const double computed = (double)(m->n_full + m->n_part) * 4096.0;
-  const double t_block = computed * d * kBlockPairPerD;
-  const double t_row = (double)m->n_valid * d * kRowPairPerD;
-  return t_row < t_block ? STA_KERNEL_ROW : STA_KERNEL_BLOCK;
+  return choose(m->n_full + m->n_part, m->n_valid, d);
+}
+
+// The choice for one mask head, when the mask carries per-head counts (else the mask's).
+bool per_head_counts(const sta_bsr_mask* m) { return m->head_tiles != nullptr && m->head_valid != nullptr; }
+int select_kernel_head(const sta_bsr_mask* m, int hm, int d, int Lk, sta_dtype dtype) {
+  if (dtype != STA_BF16 || !block_kernel_supports(d, Lk, dtype)) return STA_KERNEL_ROW;
+  if (!per_head_counts(m)) return select_kernel(m, d, Lk, dtype);
+  return choose(m->head_tiles[hm], m->head_valid[hm], d);
 }
 
 sta_status check_mask(const sta_bsr_mask* mask, int Lq, int Lk) {
@@ -105,7 +120,10 @@ extern "C" int sta_mha_select_kernel(const sta_bsr_mask* mask, int B, int H, int
   if (B < 1 || H < 1 || (d != 64 && d != 128) || (dtype != STA_BF16 && dtype != STA_F32)) return -STA_ERR_INVALID_ARG;
   const sta_status st = check_mask(mask, Lq, Lk);
   if (st != STA_OK) return -st;
-  return select_kernel(mask, d, Lk, dtype);
+  if (!per_head_counts(mask)) return select_kernel(mask, d, Lk, dtype);
+  int seen = 0;  // bit k-1: kernel k chosen for some mask head
+  for (int hm = 0; hm < mask->n_mask_heads; ++hm) seen |= 1 << (select_kernel_head(mask, hm, d, Lk, dtype) - 1);
+  return seen == 3 ? STA_KERNEL_MIXED : (seen == 2 ? STA_KERNEL_ROW : STA_KERNEL_BLOCK);
 }
 
 namespace {
@@ -139,7 +157,14 @@ sta_status mha_prepare(const sta_bsr_mask* mask, const int32_t* head_map, int B,
     std::stable_sort(a.hmap.order, a.hmap.order + H,
                      [&](uint16_t x, uint16_t y) { return w[a.hmap.m[x]] > w[a.hmap.m[y]]; });
   }
-  which = kernel == STA_KERNEL_AUTO ? select_kernel(mask, d, Lk, dtype) : kernel;
+  a.n_ranks = H;
+  if (kernel != STA_KERNEL_AUTO) {
+    which = kernel;
+  } else {
+    int seen = 0;
+    for (int h = 0; h < H; ++h) seen |= 1 << (select_kernel_head(mask, a.hmap.m[h], d, Lk, dtype) - 1);
+    which = seen == 3 ? STA_KERNEL_MIXED : (seen == 2 ? STA_KERNEL_ROW : STA_KERNEL_BLOCK);
+  }
   if (which == STA_KERNEL_BLOCK && !block_kernel_supports(d, Lk, dtype)) return STA_ERR_UNSUPPORTED;
   a.mask = MaskView{mask->full_row_ptr, mask->full_col_idx, mask->part_row_ptr, mask->part_col_idx,
                     mask->part_bitmap, static_cast<const uint8_t*>(mask->tile_lists), mask->ot_rows, mask->ot_cols,
@@ -149,6 +174,60 @@ sta_status mha_prepare(const sta_bsr_mask* mask, const int32_t* head_map, int B,
   a.B = B; a.H = H; a.Lq = Lq; a.Lk = Lk; a.d = d; a.dtype = dtype;
   a.scale_log2 = scale * kLog2e;
   return STA_OK;
+}
+
+// Under the per-head choice: the launch order split into the block-wise kernel's heads
+// (kept in their heaviest-first order) and the row-wise kernel's.
+void split_heads(const MhaArgs& a, const sta_bsr_mask* mask, MhaArgs& blk, MhaArgs& row) {
+  blk = a;
+  row = a;
+  blk.n_ranks = row.n_ranks = 0;
+  for (int r = 0; r < a.H; ++r) {
+    const int h = a.hmap.order[r];
+    if (select_kernel_head(mask, a.hmap.m[h], a.d, a.Lk, (sta_dtype)a.dtype) == STA_KERNEL_ROW)
+      row.hmap.order[row.n_ranks++] = (uint16_t)h;
+    else
+      blk.hmap.order[blk.n_ranks++] = (uint16_t)h;
+  }
+}
+
+// The library's second stream of a device (non-blocking) and the two events that fork it
+// from and join it back into a caller's stream; created on first use, kept until exit.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;  // guards the cache and each fork / join sequence
+
+sta_status side_stream(SideStream*& out) {
+  static SideStream cache[64];
+  int dev = 0;
+  STA_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return STA_ERR_UNSUPPORTED;
+  SideStream& c = cache[dev];
+  if (!c.s) {
+    STA_CUDA_TRY(cudaStreamCreateWithFlags(&c.s, cudaStreamNonBlocking));
+    STA_CUDA_TRY(cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming));
+    STA_CUDA_TRY(cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming));
+  }
+  out = &c;
+  return STA_OK;
+}
+
+// Both kernels at once: the row-wise kernel on its heads on the side stream (forked from
+// and joined back into `st`), the block-wise kernel on the others on `st`.
+sta_status launch_mixed(const MhaArgs& blk, const MhaSplit& plan, const MhaArgs& row, cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* ss = nullptr;
+  sta_status r = side_stream(ss);
+  if (r != STA_OK) return r;
+  STA_CUDA_TRY(cudaEventRecord(ss->fork, st));
+  STA_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+  r = launch_mha_row(row, ss->s);
+  STA_CUDA_TRY(cudaEventRecord(ss->join, ss->s));  // joined even after a failed launch
+  const sta_status b = launch_mha_block(blk, plan, st);
+  STA_CUDA_TRY(cudaStreamWaitEvent(st, ss->join, 0));
+  return r != STA_OK ? r : b;
 }
 
 sta_status mha_set_data(MhaArgs& a, const void* q, const void* k, const void* v, void* o, float* lse) {
@@ -172,8 +251,14 @@ extern "C" sta_status sta_mha_fwd(const void* q, const void* k, const void* v, v
   if (st != STA_OK) return st;
   if ((st = mha_set_data(a, q, k, v, o, lse)) != STA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (which != STA_KERNEL_BLOCK) return launch_mha_row(a, s);
+  if (which == STA_KERNEL_ROW) return launch_mha_row(a, s);
   MhaSplit plan;  // no split: one chunk per item
+  if (which == STA_KERNEL_MIXED) {
+    MhaArgs blk, row;
+    split_heads(a, mask, blk, row);
+    if ((st = plan_mha_split(blk, nullptr, 1, -1, plan)) != STA_OK) return st;
+    return launch_mixed(blk, plan, row, s);
+  }
   if ((st = plan_mha_split(a, nullptr, 1, -1, plan)) != STA_OK) return st;
   return launch_mha_block(a, plan, s);
 }
@@ -189,11 +274,16 @@ extern "C" sta_status sta_mha_fwd_layout(const void* q, const void* k, const voi
   sta_status st = mha_prepare(mask, head_map, B, H, Lq, Lk, d, dtype, scale, kernel, a, which);
   if (st != STA_OK) return st;
   a.o_tokens = o_layout == STA_O_BLHD ? 1 : 0;
+  if ((st = mha_set_data(a, q, k, v, o, lse)) != STA_OK && workspace) return st;
+  // the block-wise kernel's heads: all of them, or its share under the per-head choice
+  MhaArgs blk, row;
+  if (which == STA_KERNEL_MIXED) split_heads(a, mask, blk, row);
+  MhaArgs& ab = which == STA_KERNEL_MIXED ? blk : a;
   MhaSplit plan;
   size_t need = 256;  // never zero, so that a null workspace always means "query"
-  if (which == STA_KERNEL_BLOCK) {
-    if ((st = plan_mha_split(a, mask->head_tiles, num_splits, -1, plan)) != STA_OK) return st;
-    need = std::max(need, mha_split_workspace_bytes(a, plan));
+  if (which == STA_KERNEL_BLOCK || which == STA_KERNEL_MIXED) {
+    if ((st = plan_mha_split(ab, mask->head_tiles, num_splits, -1, plan)) != STA_OK) return st;
+    need = std::max(need, mha_split_workspace_bytes(ab, plan));
   }
   if (!workspace) {
     *workspace_bytes = need;
@@ -201,15 +291,15 @@ extern "C" sta_status sta_mha_fwd_layout(const void* q, const void* k, const voi
   }
   if (*workspace_bytes < need) return STA_ERR_WORKSPACE;
   if ((uintptr_t)workspace & 255u) return STA_ERR_UNSUPPORTED;
-  if ((st = mha_set_data(a, q, k, v, o, lse)) != STA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (which != STA_KERNEL_BLOCK) return launch_mha_row(a, s);
+  if (which == STA_KERNEL_ROW) return launch_mha_row(a, s);
   if (plan.n_split_ranks > 0) {
     const size_t rows = (size_t)plan.ybase[plan.n_split_ranks] * (size_t)Lq;
     plan.part_o = static_cast<float*>(workspace);
     plan.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                              (((rows * (size_t)d * sizeof(float)) + 255) & ~(size_t)255));
   }
+  if (which == STA_KERNEL_MIXED) return launch_mixed(blk, plan, row, s);
   return launch_mha_block(a, plan, s);
 }
 

@@ -577,6 +577,12 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
     long long h_tot[3] = {0, 0, 0};
     STA_CUDA_TRY(cudaMemcpyAsync(h_tot, totals, sizeof(h_tot), cudaMemcpyDeviceToHost, st));
     std::vector<int32_t> rows;
+    std::vector<unsigned long long> vrows;
+    if (out->head_valid) {  // per-head valid counts from the per-row counts of the classify pass
+      vrows.resize((size_t)Hm * R);
+      STA_CUDA_TRY(cudaMemcpyAsync(vrows.data(), vcnt, sizeof(unsigned long long) * Hm * R, cudaMemcpyDeviceToHost,
+                                   st));
+    }
     if (out->head_tiles) {  // per-head tile counts from the two row_ptr arrays
       rows.resize(2 * ((size_t)Hm * R + 1));
       STA_CUDA_TRY(cudaMemcpyAsync(rows.data(), out->full_row_ptr, sizeof(int32_t) * (Hm * R + 1),
@@ -593,6 +599,13 @@ extern "C" sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, 
       const int32_t* p = rows.data() + Hm * R + 1;
       for (int h = 0; h < Hm; ++h)
         out->head_tiles[h] = (int64_t)(f[(h + 1) * R] - f[h * R]) + (int64_t)(p[(h + 1) * R] - p[h * R]);
+    }
+    if (out->head_valid) {
+      for (int h = 0; h < Hm; ++h) {
+        unsigned long long v = 0;
+        for (int64_t a = 0; a < R; ++a) v += vrows[(size_t)h * R + a];
+        out->head_valid[h] = (int64_t)v;
+      }
     }
     return STA_OK;
   }

@@ -10,6 +10,8 @@ struct HeadMap {
   uint16_t m[kMaxHeads];      // attention head -> mask head
   uint16_t order[kMaxHeads];  // launch rank -> attention head (heaviest mask heads first)
 };
+// A launch covers the attention heads order[0 .. n_ranks-1] of the launch order: all H
+// heads, or under the per-head kernel choice the heads of one kernel.
 
 struct MhaArgs {
   const void* q;
@@ -20,6 +22,7 @@ struct MhaArgs {
   MaskView mask;
   HeadMap hmap;
   int B, H, Lq, Lk, d;
+  int n_ranks;       // heads of this launch: hmap.order[0 .. n_ranks-1]
   int dtype;
   float scale_log2;  // softmax scale * log2(e)
   int* err;          // device error word

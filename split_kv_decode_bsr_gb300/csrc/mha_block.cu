@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     rank = y / (A.B * n_split);
     off = y - rank * A.B * n_split;
   } else {
-    int lo = 0, hi = A.H;  // P.ybase[lo] <= y < P.ybase[hi]
+    int lo = 0, hi = A.n_ranks;  // P.ybase[lo] <= y < P.ybase[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (P.ybase[mid] <= y) lo = mid;
@@ -634,7 +634,7 @@ sta_status plan_mha_split(const MhaArgs& a, const int64_t* mask_head_tiles, int 
   constexpr int kMinChunk = 16;
   constexpr int kMaxAutoSplit = 32;
   constexpr double kSetupTiles = 4.0;
-  const int H = a.H, B = a.B;
+  const int H = a.n_ranks, B = a.B;  // the ranks of this launch
   p.part_o = nullptr;
   p.part_lse = nullptr;
   if (num_splits > 0) {

@@ -102,11 +102,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   using IO = RowIO<D, BF16>;
   constexpr int E = D / 32;
   __shared__ __align__(16) float s_q[kRowWarps][D];
+  __shared__ int s_keys[kRowWarps][72];  // valid keys waiting for a batch: fewer than 8, plus one tile's 64
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * kRowWarps + warp;
   if (i >= A.Lq) return;
-  const int64_t bh = blockIdx.y;
-  const int h = (int)(bh % A.H);
+  // grid.y = (batch, launch rank): the launch covers heads hmap.order[0 .. n_ranks-1]
+  const int bi = blockIdx.y / A.n_ranks;
+  const int h = A.hmap.order[blockIdx.y - bi * A.n_ranks];
+  const int64_t bh = (int64_t)bi * A.H + h;
   const int hm = A.hmap.m[h];
   const int64_t qrow = bh * A.Lq + i;
   const int64_t kv0 = bh * A.Lk;  // first K/V row of this (b, h)
@@ -169,73 +172,132 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
     }
   }
 
-  // ---- part tiles: the row's byte of each inner-tile word, four tiles per pass (lane
-  // 8u + w holds word w of tile u); the words of the next pass are requested before the
-  // keys of this one are processed
+  // ---- part tiles, 32 at a time: lane l takes part tile t0 + l and loads the row's group
+  // of its inner-tile words (eight words, 64 contiguous bytes) in four 16-byte loads, so
+  // the scan of 32 tiles costs one round trip; byte r % 8 of the eight words is the row's
+  // 64-bit key mask of that tile. The valid keys of each lane with a nonzero mask are then
+  // appended to a list in shared memory (one key per lane per step), and the list is
+  // scored NB keys at a time: every lane loads its dimensions of all NB K and V rows at
+  // once, the NB dot products are reduced together (a transpose-reduce that leaves key
+  // (lane >> (5 - LB)) of the batch on its lanes), and the running max, sum and output
+  // take one update per batch.
+  constexpr int LB = E == 2 ? 3 : 2;  // batch of NB = 2^LB keys: 8 at d = 64, 4 at d = 128
+  constexpr int NB = 1 << LB;
   const int wrow = 8 * (r >> 3), sh = (r & 7) * 8;
-  auto scan = [&](int t0, uint32_t& byte, int& col) {
-    const int tt = t0 + (lane >> 3), w = lane & 7;
-    byte = 0u;
-    col = 0;
-    if (tt < pe) {
-      byte = (uint32_t)((__ldg(A.mask.part_bitmap + (int64_t)tt * 64 + wrow + w) >> sh) & 0xFFull);
-      col = __ldg(A.mask.part_col_idx + tt);
+  int* keys = s_keys[warp];
+  const int kid = (lane >> (5 - LB)) & (NB - 1);  // key of a batch whose score this lane ends with
+  auto batch = [&](int b0, int nb) {
+    float kd[NB][E], vd[NB][E];
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+      const int64_t j = kv0 + keys[b0 + (jj < nb ? jj : 0)];
+      IO::load_lane(A.k, j, lane, kd[jj]);
+      IO::load_lane(A.v, j, lane, vd[jj]);
     }
-  };
-  uint32_t byte_next;
-  int col_next;
-  scan(pb, byte_next, col_next);
-  for (int t0 = pb; t0 < pe; t0 += 4) {
-    const uint32_t byte = byte_next;
-    const int col = col_next;
-    if (t0 + 4 < pe) scan(t0 + 4, byte_next, col_next);
-    unsigned nz = __ballot_sync(0xffffffffu, byte != 0u);
-    while (nz) {
-      const int src = __ffs(nz) - 1;
-      nz &= nz - 1;
-      uint32_t bits = __shfl_sync(0xffffffffu, byte, src);
-      // column and key clamped into the mask: a damaged mask (sta_validate_mask finds it)
-      // gives wrong values but no read outside K and V
-      const unsigned colv = min((unsigned)__shfl_sync(0xffffffffu, col, src), (unsigned)A.mask.ot_cols - 1u);
-      const int64_t base = (int64_t)colv * 64 + 8 * (src & 7);
-      while (bits) {
-        const int c = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int64_t j = kv0 + min(base + c, (int64_t)A.Lk - 1);
-        float kd[E], vd[E];
-        IO::load_lane(A.k, j, lane, kd);
-        IO::load_lane(A.v, j, lane, vd);
-        float part = 0.f;
+    float x[NB];
 #pragma unroll
-        for (int e = 0; e < E; ++e) part = fmaf(qd[e], kd[e], part);
-        const float sc = warp_sum(part);
-        if (sc > m) {  // new running max: rescale what has been accumulated (m = -inf -> 0)
-          const float alpha = exp2f(m - sc);
-          l *= alpha;
+    for (int jj = 0; jj < NB; ++jj) {
+      float part = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] *= alpha;
-          m = sc;
-        }
-        const float p = exp2f(sc - m);
-        l += p;
+      for (int e = 0; e < E; ++e) part = fmaf(qd[e], kd[jj][e], part);
+      x[jj] = part;
+    }
+    // LB halving steps at offsets 16, 8, ...: a lane keeps the half of its keys selected by
+    // its offset bit and adds the partner's copy of that half
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vd[e], acc[e]);
+    for (int st = 0; st < LB; ++st) {
+      const int off = 16 >> st, half = NB >> (st + 1);
+      const bool hi = lane & off;
+#pragma unroll
+      for (int k = 0; k < half; ++k) {
+        const float send = hi ? x[k] : x[k + half];
+        x[k] = (hi ? x[k + half] : x[k]) + __shfl_xor_sync(0xffffffffu, send, off);
       }
     }
+    float sc = x[0];
+#pragma unroll
+    for (int off = 16 >> LB; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+    if (kid >= nb) sc = -INFINITY;
+    float mb = sc;
+#pragma unroll
+    for (int off = 32 >> LB; off < 32; off <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+    const float m_new = fmaxf(m, mb);
+    const float alpha = exp2f(m - m_new);  // m = -inf -> 0
+    const float p = kid < nb ? exp2f(sc - m_new) : 0.f;
+    float ps = p;
+#pragma unroll
+    for (int off = 32 >> LB; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l = l * alpha + ps;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= alpha;
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj << (5 - LB));
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, vd[jj][e], acc[e]);
+    }
+    m = m_new;
+  };
+  int nk = 0;  // keys waiting in the list (fewer than NB after every flush)
+  for (int t0 = pb; t0 < pe; t0 += 32) {
+    const int tt = t0 + lane;
+    uint64_t bits = 0;
+    int64_t base = 0;
+    if (tt < pe) {
+      const uint4* wp = reinterpret_cast<const uint4*>(A.mask.part_bitmap + (int64_t)tt * 64 + wrow);
+      uint4 w4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) w4[u] = __ldg(wp + u);
+      // byte r % 8 of word 8p + q -> bits 8q..8q+7 of the row's mask (words q = 2u, 2u + 1)
+      const int lo_sh = sh & 31;
+      const bool upper = sh >= 32;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t b0 = ((upper ? w4[u].y : w4[u].x) >> lo_sh) & 0xFFu;
+        const uint32_t b1 = ((upper ? w4[u].w : w4[u].z) >> lo_sh) & 0xFFu;
+        bits |= (uint64_t)(b0 | (b1 << 8)) << (16 * u);
+      }
+      // column and key clamped into the mask: a damaged mask (sta_validate_mask finds it)
+      // gives wrong values but no read outside K and V
+      base = (int64_t)min((unsigned)__ldg(A.mask.part_col_idx + tt), (unsigned)A.mask.ot_cols - 1u) * 64;
+    }
+    for (unsigned nz = __ballot_sync(0xffffffffu, bits != 0ull); nz; nz &= nz - 1) {
+      const int src = __ffs(nz) - 1;
+      const uint64_t mb64 = __shfl_sync(0xffffffffu, bits, src);
+      const int64_t bs = __shfl_sync(0xffffffffu, base, src);
+      // lane c appends keys c and c + 32 of this tile when valid, in ascending order
+      const uint32_t lo = (uint32_t)mb64, hi = (uint32_t)(mb64 >> 32);
+      const uint32_t below = (1u << lane) - 1u;
+      if ((lo >> lane) & 1u) keys[nk + __popc(lo & below)] = (int)min(bs + lane, (int64_t)A.Lk - 1);
+      if ((hi >> lane) & 1u) keys[nk + __popc(lo) + __popc(hi & below)] = (int)min(bs + 32 + lane, (int64_t)A.Lk - 1);
+      nk += __popc(lo) + __popc(hi);
+      __syncwarp();
+      if (nk < NB) continue;
+      int b0 = 0;
+      for (; nk - b0 >= NB; b0 += NB) batch(b0, NB);
+      // the (fewer than NB) keys left over move to the front of the list
+      const int left = nk - b0;
+      const int kl = lane < left ? keys[b0 + lane] : 0;
+      __syncwarp();
+      if (lane < left) keys[lane] = kl;
+      nk = left;
+      __syncwarp();
+    }
   }
+  if (nk > 0) batch(0, nk);
 
   float out[E];
   const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) out[e] = acc[e] * inv;
-  IO::store_lane(A.o, o_row(A, bh / A.H, h, i), lane, out);
+  IO::store_lane(A.o, o_row(A, bi, h, i), lane, out);
   if (A.lse && lane == 0) A.lse[qrow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
 }  // namespace
 
 sta_status launch_mha_row(const MhaArgs& a, cudaStream_t st) {
-  const dim3 grid((unsigned)cdiv(a.Lq, kRowWarps), (unsigned)(a.B * a.H));
+  const dim3 grid((unsigned)cdiv(a.Lq, kRowWarps), (unsigned)(a.B * a.n_ranks));
   const dim3 block(kRowWarps * 32);
   if (a.dtype == STA_BF16) {
     if (a.d == 64) mha_row_kernel<64, true><<<grid, block, 0, st>>>(a);

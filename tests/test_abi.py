@@ -267,3 +267,27 @@ def test_bounded_wait_check_rejects_bad_limits_on_the_host(lib):
     for limit, out in ((999, 16), (2_000_000_001, 16), (-5, 16), (1_000_000, None)):
         assert lib.sta_check_bounded_wait(limit, out, None) == sta.STA_ERR_INVALID_ARG
     assert lib.sta_check_bounded_wait(1_000_000, 18, None) == sta.STA_ERR_UNSUPPORTED  # misaligned
+
+
+def test_selector_per_mask_head_on_host(lib):
+    # two mask heads at L = 4096: a 0.2 % random head (every outer tile part) and a band;
+    # with per-head counts the selector picks the row-wise kernel for the first and the
+    # block-wise kernel for the second, i.e. both
+    s = _mask_struct(Hm=2, Lq=4096, Lk=4096)
+    tiles, valid = (C.c_int64 * 2)(4096, 190), (C.c_int64 * 2)(33554, 520000)
+    s.n_full, s.n_part, s.n_valid = 64, 4222, 553554
+    s.full_col_idx = s.part_col_idx = s.part_bitmap = 16  # never dereferenced by the selector
+    s.head_tiles = C.cast(tiles, C.c_void_p)
+    s.head_valid = C.cast(valid, C.c_void_p)
+    assert lib.sta_mha_select_kernel(C.byref(s), 1, 2, 4096, 4096, 64, sta.STA_BF16) == sta.STA_KERNEL_MIXED
+    # both heads sparse: row; both structured: block
+    valid[1] = 1000
+    assert lib.sta_mha_select_kernel(C.byref(s), 1, 2, 4096, 4096, 64, sta.STA_BF16) == sta.STA_KERNEL_ROW
+    valid[0], valid[1] = 4_000_000, 520000
+    assert lib.sta_mha_select_kernel(C.byref(s), 1, 2, 4096, 4096, 64, sta.STA_BF16) == sta.STA_KERNEL_BLOCK
+    # without per-head counts: one choice from the totals
+    s.head_valid = None
+    assert lib.sta_mha_select_kernel(C.byref(s), 1, 2, 4096, 4096, 64, sta.STA_BF16) == sta.STA_KERNEL_BLOCK
+    # fp32 runs on the row-wise kernel only
+    s.head_valid = C.cast(valid, C.c_void_p)
+    assert lib.sta_mha_select_kernel(C.byref(s), 1, 2, 4096, 4096, 64, sta.STA_F32) == sta.STA_KERNEL_ROW

@@ -125,3 +125,79 @@ def test_mixed_heads_more_tiles_than_resident_ctas(dev):
     heads = [W.MaskHead("u8", data=u8), W.pattern(causal=True), W.pattern(win_lo=-40, win_hi=40)]
     head_map = [h % 3 for h in range(H)]
     _run(q, k, v, heads, head_map, 0.125, "bf16", "block", dev, L, L)
+
+
+def _mixed_heads(L, density, seed=31):
+    u8 = W.random_mask_u8(seed, 7, L, L, density)
+    return [W.pattern(win_lo=-64, win_hi=64), W.MaskHead("bits", data=W.pack_bits(u8)),
+            W.pattern(causal=True, win_lo=-200, n_global_cols=8)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_per_head_choice_runs_both_kernels(dev, d):
+    # structured heads (band, causal window + global columns) with one 0.2 % random head:
+    # the per-head selector sends the random head to the row-wise kernel and the rest to the
+    # block-wise kernel, concurrently; every row against the oracle, through sta_mha_fwd and
+    # through sta_mha_fwd_splitkv (forced chunks for the block heads, O token-major)
+    import split_kv_decode_bsr_gb300 as sta
+
+    B, H, L = 2, 6, 1000
+    heads = _mixed_heads(L, 0.002)
+    head_map = [0, 1, 2, 0, 2, 0]
+    q = W.make_tensor(30, 1, (B, H, L, d), "bf16")
+    k = W.make_tensor(30, 2, (B, H, L, d), "bf16")
+    v = W.make_tensor(30, 3, (B, H, L, d), "bf16")
+    mask = sta.sta_encode_mask(gpu_sources(heads, dev), L, L)
+    assert sta.sta_mha_select_kernel(mask, B, H, d) == "mixed"
+    o_ref, lse_ref = oracle.mha_fwd(q.f32, k.f32, v.f32, heads, head_map, 1.0 / math.sqrt(d))
+    tq, tk, tv = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
+    o, lse = sta.sta_mha_fwd(tq, tk, tv, mask, head_map=head_map)
+    assert sta.sta_device_error() == 0
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16", "mixed")
+    o, lse = sta.sta_mha_fwd_splitkv(tq, tk, tv, mask, head_map=head_map, num_splits=3, o_layout="blhd")
+    assert sta.sta_device_error() == 0
+    compare(o.permute(0, 2, 1, 3).float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16", "mixed split")
+    # without the per-head counts the choice is made once for the whole mask
+    mask.head_valid = None
+    assert sta.sta_mha_select_kernel(mask, B, H, d) in ("block", "row")
+
+
+def test_per_head_choice_inside_a_cuda_graph(dev):
+    # the fork to the library's second stream and the join back are captured with the call;
+    # two replays on fresh inputs match the oracle
+    import torch
+
+    import split_kv_decode_bsr_gb300 as sta
+
+    B, H, L, d = 1, 4, 700, 64
+    heads = _mixed_heads(L, 0.002, seed=32)
+    head_map = [0, 1, 2, 1]
+    mask = sta.sta_encode_mask(gpu_sources(heads, dev), L, L)
+    assert sta.sta_mha_select_kernel(mask, B, H, d) == "mixed"
+    bufs = [torch.empty((B, H, L, d), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    o = torch.empty_like(bufs[0])
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        sta.sta_mha_fwd(*bufs, mask, head_map=head_map, o=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sta.sta_mha_fwd(*bufs, mask, head_map=head_map, o=o, lse=lse)
+    for seed in (33, 34):
+        ins = [W.make_tensor(seed, s, (B, H, L, d), "bf16") for s in (1, 2, 3)]
+        for b, t in zip(bufs, ins):
+            b.copy_(to_dev(t, dev))
+        g.replay()
+        torch.cuda.synchronize()
+        o_ref, lse_ref = oracle.mha_fwd(ins[0].f32, ins[1].f32, ins[2].f32, heads, head_map, 1.0 / math.sqrt(d))
+        compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16", f"graph replay {seed}")
+    assert sta.sta_device_error() == 0
+
+
+def test_mixed_sparse_workload_every_row(dev):
+    # the bench's mixed workload (15 band heads, one 0.2 % random head) through the bench's call
+    wl = W.mixed_sparse()
+    _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "bf16", "auto", dev, wl.Lq, wl.Lk)

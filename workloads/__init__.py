@@ -315,6 +315,20 @@ def sparse_random(seed: int = 0, B: int = 1, H: int = 8, L: int = 4096, d: int =
                        {"mask": f"i.i.d. Bernoulli({density:g}) per element, one mask head for all heads"})
 
 
+def mixed_sparse(seed: int = 0, B: int = 1, H: int = 16, L: int = 4096, d: int = 64, w: int = 64,
+                 density: float = 0.002) -> MhaWorkload:
+    """Structured heads with one very sparse head, bf16: heads 0..H-2 share the band |i - j| <= w,
+    head H-1 uses an i.i.d. Bernoulli(density) mask (draw i * L + j of the mask-element stream).
+    The band suits the block-wise kernel, the sparse head the row-wise one."""
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16")
+    band = pattern(win_lo=-w, win_hi=w)
+    rnd = MaskHead("bits", data=random_mask_bits(seed, STREAM_MASK_ELEMS, L, L, density))
+    return MhaWorkload(f"mixed-sparse bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       [band, rnd], [0] * (H - 1) + [1], 1.0 / math.sqrt(d),
+                       {"mask": f"heads 0..{H - 2}: |i-j| <= {w}; head {H - 1}: i.i.d. Bernoulli({density:g}) "
+                                "per element"})
+
+
 def bigbird_blocks(seed: int, Hm: int, L: int, blk: int = 64, n_rand: int = 3):
     """Per mask head and query block: the sorted key-block lists of the BigBird recipe.
 
