@@ -602,13 +602,11 @@ def mha_roofline(b, t, peaks, traffic, which):
 
 
 def summary_entry(d):
-    """value, unit, roofline fraction (with its bound) and ms of one workload object."""
+    """[value, unit, ms, roofline fraction, bound] of one workload object (the last two null
+    without a roofline)."""
     r = d.get("roofline") or {}
-    e = {"value": round(d["value"], 4), "unit": d["unit"], "ms": round(d["ms_per_step"], 5)}
-    if r:
-        e["frac"] = round(r["frac"], 4)
-        e["bound"] = r["bound"]
-    return e
+    return [round(d["value"], 2), d["unit"], round(d["ms_per_step"], 4), round(r["frac"], 3) if r else None,
+            r.get("bound")]
 
 
 def measure_mha(name, dev, args, dist, flush, peaks, peak_src, steps):
@@ -825,7 +823,7 @@ def main():
     if err:
         line["device_error"] = err
     # last key: one short entry per workload, so the end of the line holds every figure
-    line["summary"] = summary
+    line["summary"] = dict(summary, columns=["value", "unit", "ms", "frac", "bound"])
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
