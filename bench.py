@@ -234,7 +234,8 @@ def mha_workload(name):
     return {"bert-band": W.bert_band, "bigbird": W.bigbird, "longformer": W.longformer,
             "tiny-causal": W.tiny_causal, "long-causal": W.long_causal,
             "causal-1head": lambda: W.long_causal(H=1, L=16384), "sparse-random": W.sparse_random,
-            "mixed-sparse": W.mixed_sparse}[name]()
+            "mixed-sparse": W.mixed_sparse, "dense-square": lambda: W.square_mask("dense"),
+            "part-square": lambda: W.square_mask("random")}[name]()
 
 
 def algorithmic_bytes_mha(wl, mask):
@@ -661,6 +662,7 @@ def measure_mha(name, dev, args, dist, flush, peaks, peak_src, steps):
         "ms_per_step": 1e3 * t, "config": mha_config(b.wl, b.pairs, dist.world),
         "launch": {"kernel": b.kernel, "split_kv": "planned" if b.split else "none", "workspace_bytes": b.ws.numel()},
         "tensor_frac": (b.flops / t / 1e12) / peaks["bf16_tflops"],
+        "tensor_frac_sustained": (b.flops / t / 1e12) / peaks["bf16_tflops_sustained"],
         "roofline": mha_roofline(b, t, peaks, recorded_traffic(kf, name), peak_src),
         "gpu_launches": b.launches_per_step() * steps,
         "timing_stats": timing_stats(ms, g, steps, args.warmup, dist),
@@ -680,7 +682,7 @@ def main():
                                        "sparse-random,mixed-sparse,epilogue-ln,mha-token-major,mla-decode",
                     help="comma list of secondary workloads (bert-band, bigbird, longformer, decode, decode-paged, "
                          "long-causal, causal-1head, sparse-random, mixed-sparse, epilogue-ln, mha-token-major, "
-                         "mla-decode) or 'none'")
+                         "mla-decode, and the matched pair dense-square / part-square) or 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--mha-splits", type=int, default=0,
                     help="split-KV chunks per head for the block kernel (0: the library's plan)")
@@ -734,6 +736,7 @@ def main():
         "config": head["config"],
         "launch": dict(head["launch"], timing="CUDA events around a CUDA-graph replay of one library call per step"),
         "tensor_frac": head["tensor_frac"],
+        "tensor_frac_sustained": head["tensor_frac_sustained"],
         "roofline": head["roofline"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": mb.h2d_bytes,
                 "d2h_bytes_per_step": mb.d2h_bytes,

@@ -315,6 +315,21 @@ def sparse_random(seed: int = 0, B: int = 1, H: int = 8, L: int = 4096, d: int =
                        {"mask": f"i.i.d. Bernoulli({density:g}) per element, one mask head for all heads"})
 
 
+def square_mask(kind: str, seed: int = 0, B: int = 1, H: int = 32, L: int = 4096, d: int = 128,
+                density: float = 0.5) -> MhaWorkload:
+    """Matched pair for the block-wise kernel's tile cost: kind "dense" is the all-ones mask
+    (every outer tile full), kind "random" an i.i.d. Bernoulli(density) mask (every outer
+    tile part) over the same shape and values (N(0, 1) * 0.5, bf16)."""
+    q, k, v = _qkv(seed, B, H, L, L, d, "bf16", mult=0.5)
+    if kind == "dense":
+        head, desc = pattern(), "all ones"
+    else:
+        head = MaskHead("bits", data=random_mask_bits(seed, STREAM_MASK_ELEMS, L, L, density))
+        desc = f"i.i.d. Bernoulli({density:g}) per element"
+    return MhaWorkload(f"{kind}-square bf16 B{B} H{H} L{L} d{d}", B, H, L, L, d, "bf16", q, k, v,
+                       [head], [0] * H, 1.0 / math.sqrt(d), {"mask": desc})
+
+
 def mixed_sparse(seed: int = 0, B: int = 1, H: int = 16, L: int = 4096, d: int = 64, w: int = 64,
                  density: float = 0.002) -> MhaWorkload:
     """Structured heads with one very sparse head, bf16: heads 0..H-2 share the band |i - j| <= w,
