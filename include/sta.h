@@ -253,10 +253,11 @@ sta_status sta_encode_mask(const sta_mask_src* srcs, int Hm, int Lq, int Lk, sta
  *            per mask head when mask->head_tiles and mask->head_valid are both
  *            set, else once for the whole mask. When the per-head choice picks
  *            both kernels, the row-wise kernel runs on its heads on a stream of
- *            the library's own (created on the first such call on a device,
- *            forked from and joined back into `stream` with events, so the call
- *            stays asynchronous and can be captured in a CUDA graph) while the
- *            block-wise kernel runs on the others on `stream`.
+ *            the library's own (one per host thread and device, created on the
+ *            first such call, forked from and joined back into `stream` with
+ *            events, so the call stays asynchronous and can be captured in a
+ *            CUDA graph) while the block-wise kernel runs on the others on
+ *            `stream`.
  * Pointers must be 16-byte aligned. Asynchronous on `stream`. */
 sta_status sta_mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const sta_bsr_mask* mask,
                        const int32_t* head_map, int B, int H, int Lq, int Lk, int d, sta_dtype dtype, float scale,

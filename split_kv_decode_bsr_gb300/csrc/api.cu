@@ -192,15 +192,16 @@ void split_heads(const MhaArgs& a, const sta_bsr_mask* mask, MhaArgs& blk, MhaAr
 }
 
 // The library's second stream of a device (non-blocking) and the two events that fork it
-// from and join it back into a caller's stream; created on first use, kept until exit.
+// from and join it back into a caller's stream; one set per host thread and device, created
+// on first use and kept until exit. Per thread, so that a capture in progress on one thread
+// (which holds the side stream until the capture ends) cannot take in another thread's work.
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-std::mutex g_side_mu;  // guards the cache and each fork / join sequence
 
 sta_status side_stream(SideStream*& out) {
-  static SideStream cache[64];
+  thread_local SideStream cache[64];
   int dev = 0;
   STA_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return STA_ERR_UNSUPPORTED;
@@ -217,7 +218,6 @@ sta_status side_stream(SideStream*& out) {
 // Both kernels at once: the row-wise kernel on its heads on the side stream (forked from
 // and joined back into `st`), the block-wise kernel on the others on `st`.
 sta_status launch_mixed(const MhaArgs& blk, const MhaSplit& plan, const MhaArgs& row, cudaStream_t st) {
-  std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* ss = nullptr;
   sta_status r = side_stream(ss);
   if (r != STA_OK) return r;

@@ -201,3 +201,46 @@ def test_mixed_sparse_workload_every_row(dev):
     # the bench's mixed workload (15 band heads, one 0.2 % random head) through the bench's call
     wl = W.mixed_sparse()
     _run(wl.q, wl.k, wl.v, wl.mask_heads, wl.head_map, wl.scale, "bf16", "auto", dev, wl.Lq, wl.Lk)
+
+
+def test_per_head_choice_from_two_host_threads(dev):
+    # two host threads issue mixed calls at once, each on its own stream (each thread gets its
+    # own side stream); both results match the oracle
+    import threading
+
+    import torch
+
+    import split_kv_decode_bsr_gb300 as sta
+
+    B, H, L, d = 1, 4, 600, 64
+    heads = _mixed_heads(L, 0.002, seed=35)
+    head_map = [0, 1, 2, 1]
+    mask = sta.sta_encode_mask(gpu_sources(heads, dev), L, L)
+    assert sta.sta_mha_select_kernel(mask, B, H, d) == "mixed"
+    ins = [[W.make_tensor(40 + t, s, (B, H, L, d), "bf16") for s in (1, 2, 3)] for t in range(2)]
+    outs, errs = [None, None], []
+
+    def work(t):
+        try:
+            torch.cuda.set_device(dev)
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                q, k, v = (to_dev(x, dev) for x in ins[t])
+                for _ in range(5):
+                    o, lse = sta.sta_mha_fwd(q, k, v, mask, head_map=head_map, stream=st)
+                st.synchronize()
+                outs[t] = (o.float().cpu().numpy(), lse.cpu().numpy())
+        except Exception as e:  # reported below
+            errs.append(e)
+
+    th = [threading.Thread(target=work, args=(t,)) for t in range(2)]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    assert not errs, errs
+    for t in range(2):
+        o_ref, lse_ref = oracle.mha_fwd(ins[t][0].f32, ins[t][1].f32, ins[t][2].f32, heads, head_map,
+                                        1.0 / math.sqrt(d))
+        compare(outs[t][0], outs[t][1], o_ref, lse_ref, "bf16", f"thread {t}")
+    assert sta.sta_device_error() == 0
