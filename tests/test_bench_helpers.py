@@ -50,3 +50,21 @@ def test_recorded_traffic_needs_the_matching_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("epilogue.cu", "epilogue-ln") == 361614080.0
     assert bench.recorded_traffic("epilogue.cu", "other") is None  # recorded on other code
     assert bench.recorded_traffic("epilogue.cu", "missing") is None
+
+
+def test_summary_entry_is_short_and_keeps_the_roofline():
+    d = {"value": 284.38355, "unit": "TFLOP/s", "ms_per_step": 0.27083,
+         "roofline": {"frac": 0.31215, "bound": "hbm"}}
+    assert bench.summary_entry(d) == [284.38, "TFLOP/s", 0.2708, 0.312, "hbm"]
+    assert bench.summary_entry({"value": 1.0, "unit": "GB/s", "ms_per_step": 2.0}) == [1.0, "GB/s", 2.0, None, None]
+
+
+def test_both_arms_describe_the_workload_alike():
+    # the reference arm and the GPU arm report the same config dict for a workload
+    import workloads as W
+
+    wl = W.bert_band()
+    c = bench.mha_config(wl, 96 * 61888, 1)
+    assert c["workload"] == wl.name and c["mask"] == "sliding window |i-j| <= 64" and c["valid_pairs"] == 96 * 61888
+    assert c["L"] == 512 and c["d"] == 64 and c["parallelism"] == "replicas x1"
+    assert bench.mha_config(wl, 96 * 61888, 1) == c
