@@ -206,10 +206,18 @@ sta_status side_stream(SideStream*& out) {
   STA_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return STA_ERR_UNSUPPORTED;
   SideStream& c = cache[dev];
-  if (!c.s) {
-    STA_CUDA_TRY(cudaStreamCreateWithFlags(&c.s, cudaStreamNonBlocking));
-    STA_CUDA_TRY(cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming));
-    STA_CUDA_TRY(cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming));
+  if (!c.s) {  // all three or none: a failed creation leaves nothing half made
+    SideStream n;
+    cudaError_t e = cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      if (n.fork) cudaEventDestroy(n.fork);
+      if (n.s) cudaStreamDestroy(n.s);
+      note_cuda_error(e);
+      return STA_ERR_CUDA;
+    }
+    c = n;
   }
   out = &c;
   return STA_OK;
