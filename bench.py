@@ -374,7 +374,7 @@ class DecodeBench:
         self.bytes = self.kv_bytes + 2 * wl.n_req * wl.Hq * wl.d * 2 + wl.n_req * wl.Hq * 4
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty((wl.n_req, wl.Hq), dtype=torch.float32, device=dev)
-        nbytes = sta.decode_workspace_bytes(self.ind_host, wl.n_req, wl.Hq, wl.Hkv, wl.d, 0)
+        nbytes = sta.decode_workspace_bytes(self.ind_host, wl.n_req, wl.Hq, wl.Hkv, wl.d, 0, page_size)
         self.ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
         self.page_size = page_size
         if page_size:  # the same K/V values in pages of page_size tokens, in a random page order

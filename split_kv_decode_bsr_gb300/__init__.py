@@ -471,12 +471,18 @@ def _indptr_host(kv_indptr) -> "C.Array":
     return (C.c_int32 * len(vals))(*[int(x) for x in vals])
 
 
-def decode_workspace_bytes(kv_indptr, n_req, Hq, Hkv, d, num_splits=0) -> int:
-    """Workspace size sta_decode_splitkv needs for these requests (host only)."""
+def decode_workspace_bytes(kv_indptr, n_req, Hq, Hkv, d, num_splits=0, page_size=0) -> int:
+    """Workspace size sta_decode_splitkv (page_size 0) or sta_decode_splitkv_paged needs for these
+    requests (host only)."""
     n = C.c_size_t(0)
     ind = _indptr_host(kv_indptr)
-    _check("sta_decode_splitkv", lib().sta_decode_splitkv(None, None, None, None, ind, n_req, Hq, Hkv, d, STA_BF16,
-                                                           1.0, num_splits, None, None, None, C.byref(n), None))
+    if page_size:
+        _check("sta_decode_splitkv_paged",
+               lib().sta_decode_splitkv_paged(None, None, None, page_size, 0, None, None, None, ind, n_req, Hq, Hkv, d,
+                                              STA_BF16, 1.0, num_splits, None, None, None, C.byref(n), None))
+    else:
+        _check("sta_decode_splitkv", lib().sta_decode_splitkv(None, None, None, None, ind, n_req, Hq, Hkv, d, STA_BF16,
+                                                               1.0, num_splits, None, None, None, C.byref(n), None))
     return int(n.value)
 
 

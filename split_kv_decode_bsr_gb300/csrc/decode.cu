@@ -1,22 +1,25 @@
-// Split-KV GQA decode and log-sum-exp merge (Cleave, Split演算子によるSplit-Kの対応:
-// a Split operator with a split count s parallelises the KV reduction; each
-// chunk is attended on its own and the partial softmax results are merged).
+// Split-KV GQA decode and log-sum-exp merge (Cleave, the Split operator: a split count s
+// parallelises the reduction over the KV tokens; each chunk is attended on its own and the
+// partial softmax results are merged by their log-sum-exp).
 //
-// Decode kernel: persistent-style CTAs, each owning a list of KV segments
-// (request r, token range [a, b)) and a block of HB kv heads. One producer warp
-// streams K/V tiles (NT tokens x HB heads x d, bf16) from HBM into a ring of
-// shared-memory stages with 1-D bulk copies completing on mbarriers; HB consumer
-// warps (one per kv head) score the G query heads of their group against each
-// tile on the FMA pipe (lanes own d/32 dimensions; a 32-way reduce-scatter over
-// shuffles turns per-lane partial dot products into one full score per lane),
-// run an fp32 online softmax per query head, and accumulate P.V. A segment that
-// covers its whole request writes O (bf16) and LSE directly; otherwise it writes
-// a normalised fp32 partial and its LSE, merged afterwards.
+// Decode kernel: persistent-style CTAs, each owning a list of KV segments (request r, token
+// range [a, b)) and a block of HB kv heads. One producer warp streams K/V tiles (16 tokens x HB
+// heads x d, bf16) from HBM into a ring of shared-memory stages with 1-D bulk copies, one per
+// token row, completing on mbarriers; packed and paged K/V differ only in where a row is read
+// from. HB consumer warps (one per kv head) compute on the tensor cores with
+// mma.sync.m16n8k16 (bf16 operands, fp32 accumulators): the warp's G query heads are the M of
+// the MMA (rows G..15 are zero), S[16 x 16 tokens] = Q K^T takes d / 16 k-steps over K rows
+// read by ldmatrix, the fp32 online softmax runs on the accumulator fragments (a quad of
+// lanes holds a row), P passes from the S fragments straight into the A fragments of P V, and
+// O[16 x d] accumulates in registers over V rows read by ldmatrix .trans. Token rows are
+// padded by 16 bytes in shared memory so that the eight rows one ldmatrix reads fall in
+// distinct banks. A segment that covers its whole request writes O (bf16) and LSE directly;
+// otherwise it writes a normalised fp32 partial and its LSE, merged afterwards.
 //
-// Split plans: mode 0 cuts the concatenated token stream [0, T) into equal
-// ranges, one per CTA (balanced work whatever the length mix; partial slot of
-// (CTA x, request r) = x + r, unique because both grow along the stream);
-// mode 1 cuts every request into s chunks of ceil(len / s) keys (slot r*s + c).
+// Split plans: mode 0 cuts the concatenated token stream [0, T) into equal ranges, one per
+// CTA (balanced work whatever the length mix; partial slot of (CTA x, request r) = x + r,
+// unique because both grow along the stream); mode 1 cuts every request into s chunks of
+// ceil(len / s) keys (slot r*s + c).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -29,19 +32,16 @@ struct StageInfo {
   int r, tok0, n, flags, slot;
 };
 
+constexpr int kNT = 16;  // tokens per tile
+
 template <int G, int D, int HB>
 struct DecCfg {
-  static constexpr int E = D / 32;
-  static constexpr int TG = 32 / G;             // tokens per reduce-scatter group
-  static constexpr int NT = TG > 8 ? TG : 8;    // tokens per tile
-  static constexpr int GROUPS = NT / TG;
-  static constexpr int TILE_BYTES = NT * HB * D * 2;  // K or V part of one stage
-  // ~96 KiB of stages so that two CTAs (16 consumer warps) share an SM
-  static constexpr int STAGES_RAW = 98304 / (2 * TILE_BYTES);
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : (STAGES_RAW < 2 ? 2 : STAGES_RAW);
-  static_assert(2 * STAGES * TILE_BYTES <= 200 * 1024, "decode stages exceed shared memory");
-  static constexpr int SMEM = STAGES * 2 * TILE_BYTES;
+  static constexpr int ROW = HB * D * 2 + 16;  // padded bytes of one token's HB heads
+  static constexpr int TILE = kNT * ROW;       // K or V part of one stage
+  static constexpr int STAGES = 3;
+  static constexpr int SMEM = STAGES * 2 * TILE;
   static constexpr int THREADS = (HB + 1) * 32;
+  static_assert(SMEM <= 110 * 1024, "two CTAs per SM");
 };
 
 // Largest r with indptr[r] <= t (indptr non-decreasing, indptr[0] = 0 <= t).
@@ -68,19 +68,73 @@ __device__ __forceinline__ void request_range(const DecodeArgs& A, int r, int& r
   }
 }
 
+// Page table lookups of the paged layout, made by the producer warp: lane l holds the page
+// number of ordinal base + l of request r (warp-uniform bookkeeping; reloaded when a lookup
+// leaves the window of 32 ordinals).
+struct PageCache {
+  int r = -1, base = 0, page = 0, rb = 0, pb = 0, pe = 0;
+
+  __device__ void load(const DecodeArgs& A, int req, int b, int lane) {
+    if (req != r) {
+      r = req;
+      int re_unused;
+      request_range(A, req, rb, re_unused);  // the same clamped start the token ranges use
+      pb = __ldg(A.page_indptr + req);
+      pe = __ldg(A.page_indptr + req + 1);
+    }
+    base = b;
+    const int o = pb + b + lane;
+    page = o < pe ? __ldg(A.page_indices + o) : 0;
+  }
+  // first token of request req
+  __device__ int start(const DecodeArgs& A, int req, int lane) {
+    if (req != r) load(A, req, 0, lane);
+    return rb;
+  }
+  // page of this lane's ordinal `mine` in the warp-uniform range [lo, hi] (hi - lo < 32); a
+  // page number outside the cache reads page 0 and reports 0x110
+  __device__ int lookup(const DecodeArgs& A, int req, int lo, int hi, int mine, int lane) {
+    if (req != r || lo < base || hi >= base + 32) load(A, req, lo, lane);
+    int pg = __shfl_sync(0xffffffffu, page, mine - base);
+    if (pg < 0 || pg >= A.n_pages) {
+      record_error(A.err, 0x110);
+      pg = 0;
+    }
+    return pg;
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// D += A (16 x 16, row) * B (16 x 8, col); bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 template <int G, int D, int HB>
-__global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const DecodeArgs A) {
+__global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(const DecodeArgs A) {
   using Cfg = DecCfg<G, D, HB>;
-  constexpr int E = Cfg::E, TG = Cfg::TG, NT = Cfg::NT, STAGES = Cfg::STAGES;
+  constexpr int STAGES = Cfg::STAGES, KS = D / 16, NB = D / 8;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
   __shared__ StageInfo info[STAGES];
-  __shared__ __align__(16) float s_p[HB][TG * G];
-  __shared__ float s_alpha[HB][G];
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g0 = blockIdx.y * HB;  // first kv head of this CTA
   const int Hkv = A.Hkv;
+  // rows past a tile's tokens are never copied and must hold finite values (weights 0)
+  for (int i = threadIdx.x; i < Cfg::SMEM / 16; i += blockDim.x) reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -88,6 +142,7 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
     }
     fence_mbar_init();
   }
+  fence_proxy_async_smem();  // the zero stores come before any bulk copy into those rows
   __syncthreads();
 
   if (warp == HB) {
@@ -95,42 +150,7 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
-    // Page cache of the paged layout: lane l holds the page number of ordinal pc_base + l of
-    // request pc_r (warp-uniform bookkeeping; reloaded when a lookup leaves the window).
-    int pc_r = -1, pc_base = 0, pc_page = 0, pc_rb = 0, pc_pb = 0, pc_pe = 0;
-    auto pc_load = [&](int r, int base) {
-      if (r != pc_r) {
-        pc_r = r;
-        int re_unused;
-        request_range(A, r, pc_rb, re_unused);  // the same clamped start the token ranges use
-        pc_pb = __ldg(A.page_indptr + r);
-        pc_pe = __ldg(A.page_indptr + r + 1);
-      }
-      pc_base = base;
-      const int o = pc_pb + base + lane;
-      pc_page = o < pc_pe ? __ldg(A.page_indices + o) : 0;
-    };
-    auto pc_start = [&](int r) {
-      if (r != pc_r) pc_load(r, 0);
-      return pc_rb;
-    };
-    auto checked = [&](int pg) {
-      if (pg < 0 || pg >= A.n_pages) {  // a bad page table: read page 0, report
-        record_error(A.err, 0x110);
-        pg = 0;
-      }
-      return pg;
-    };
-    // page number of ordinal `ord` (warp-uniform) of request r
-    auto page_of = [&](int r, int ord) {
-      if (r != pc_r || ord < pc_base || ord >= pc_base + 32) pc_load(r, ord);
-      return checked(__shfl_sync(0xffffffffu, pc_page, ord - pc_base));
-    };
-    // per-lane ordinal `mine` within the warp-uniform range [lo, hi] (hi - lo < 32)
-    auto pages_for_stage = [&](int r, int lo, int hi, int mine) {
-      if (r != pc_r || lo < pc_base || hi >= pc_base + 32) pc_load(r, lo);
-      return checked(__shfl_sync(0xffffffffu, pc_page, mine - pc_base));
-    };
+    PageCache pc;
     auto emit = [&](int r, int a, int n, int flags, int slot) -> bool {
       if (lane == 0) ok = mbar_wait(&empty_bar[stage], (round & 1u) ^ 1u, A.err, 0x101);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -141,58 +161,33 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
         else mbar_arrive(&full_bar[stage]);
       }
       __syncwarp();
-      if (n > 0) {
-        uint8_t* ks = smem + (size_t)stage * 2 * Cfg::TILE_BYTES;
-        uint8_t* vs = ks + Cfg::TILE_BYTES;
-        const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(A.k);
-        const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(A.v);
-        if (A.page_size == 0) {
-          if (HB == Hkv) {
-            if (lane == 0) {
-              const size_t off = (size_t)a * Hkv * D;
-              bulk_g2s(ks, kg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
-              bulk_g2s(vs, vg + off, (uint32_t)(n * HB * D * 2), &full_bar[stage]);
-            }
-          } else if (lane < n) {
-            const size_t off = ((size_t)(a + lane) * Hkv + g0) * D;
-            bulk_g2s(ks + lane * HB * D * 2, kg + off, HB * D * 2, &full_bar[stage]);
-            bulk_g2s(vs + lane * HB * D * 2, vg + off, HB * D * 2, &full_bar[stage]);
-          }
-        } else {
-          // paged K/V: tokens a .. a+n-1 of request r, copied page run by page run; the page
-          // numbers come from the warp's page cache (all lanes take part in the lookups)
-          const int P = A.page_size;
-          const int rel0 = a - pc_start(r);  // position of token a within its request
-          if (HB == Hkv) {
-            for (int t = 0; t < n;) {
-              const int rel = rel0 + t;
-              const int run = min(n - t, P - rel % P);
-              const size_t off = ((size_t)page_of(r, rel / P) * P + rel % P) * Hkv * D;
-              if (lane == 0) {
-                bulk_g2s(ks + t * HB * D * 2, kg + off, (uint32_t)(run * HB * D * 2), &full_bar[stage]);
-                bulk_g2s(vs + t * HB * D * 2, vg + off, (uint32_t)(run * HB * D * 2), &full_bar[stage]);
-              }
-              t += run;
-            }
-          } else {
-            const int rel = rel0 + min(lane, n - 1);
-            const int pg = pages_for_stage(r, rel0 / P, (rel0 + n - 1) / P, rel / P);
-            if (lane < n) {
-              const size_t off = (((size_t)pg * P + rel % P) * Hkv + g0) * D;
-              bulk_g2s(ks + lane * HB * D * 2, kg + off, HB * D * 2, &full_bar[stage]);
-              bulk_g2s(vs + lane * HB * D * 2, vg + off, HB * D * 2, &full_bar[stage]);
-            }
-          }
-        }
+      // lane l < 16 copies token a + l's K row, lane 16 + l its V row
+      const int tok = lane & 15;
+      size_t row;  // token row (HB heads from g0) in K / V, in elements
+      if (A.page_size == 0) {
+        row = ((size_t)(a + tok) * Hkv + g0) * D;
+      } else {
+        // token a + tok of request r sits at slot rel % P of the request's page rel / P; every
+        // lane takes part in the lookup (lanes past n look up the tile's last token)
+        const int P = A.page_size;
+        const int rel0 = n > 0 ? a - pc.start(A, r, lane) : 0;
+        const int rel = rel0 + min(tok, max(n - 1, 0));
+        const int pg = n > 0 ? pc.lookup(A, r, rel0 / P, (rel0 + n - 1) / P, rel / P, lane) : 0;
+        row = (((size_t)pg * P + rel % P) * Hkv + g0) * D;
+      }
+      if (tok < n) {
+        uint8_t* dst = smem + (size_t)stage * 2 * Cfg::TILE + (lane >> 4) * Cfg::TILE + tok * Cfg::ROW;
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(lane < 16 ? A.k : A.v);
+        bulk_g2s(dst, src + row, HB * D * 2, &full_bar[stage]);
       }
       if (++stage == STAGES) { stage = 0; ++round; }
       return true;
     };
     auto emit_segment = [&](int r, int a, int b, bool final, int slot) -> bool {
       if (a >= b) return emit(r, a, 0, kFirst | kLast | (final ? kFinal : 0), slot);
-      for (int t = a; t < b; t += NT) {
-        const int n = min(NT, b - t);
-        const int flags = (t == a ? kFirst : 0) | (t + NT >= b ? kLast : 0) | (final ? kFinal : 0);
+      for (int t = a; t < b; t += kNT) {
+        const int n = min(kNT, b - t);
+        const int flags = (t == a ? kFirst : 0) | (t + kNT >= b ? kLast : 0) | (final ? kFinal : 0);
         if (!emit(r, t, n, flags, slot)) return false;
       }
       return true;
@@ -231,147 +226,110 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS) decode_kernel(const
   }
 
   // -------------------------------------------------------------- consumers
-  const int g = g0 + warp;  // kv head of this warp
+  const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates: rows g, g + 8; columns 2t, 2t + 1
+  const int kvh = g0 + warp;              // kv head of this warp
   const int Hq = A.Hq;
-  // q and the output accumulators as packed fp32 pairs (dims 2e, 2e+1 of this lane's E)
-  constexpr int E2 = E / 2;
-  uint64_t q2[G][E2], acc2[G][E2];
-  float m_l = -INFINITY, l_l = 0.f;  // running max / sum of head (lane / TG)
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t qa[KS][4];
+  float oacc[NB][4];
+  float m_r = -INFINITY, l_r = 0.f;  // running max of row g, this lane's share of its sum
   int stage = 0;
   uint32_t round = 0;
-  const int my_h = lane / TG, my_t = lane % TG;
   for (;;) {
     if (!mbar_wait(&full_bar[stage], round & 1u, A.err, 0x102)) break;
     const StageInfo inf = info[stage];
     if (inf.flags & kDone) break;
     if (inf.flags & kFirst) {
-      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(A.q) + ((size_t)inf.r * Hq + (size_t)g * G) * D;
-      const uint64_t sc2 = f32x2_pack(A.scale_log2, A.scale_log2);
+      // query rows of this warp's G heads as mma A fragments (row g: head g; rows >= G zero)
+      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(A.q) + ((size_t)inf.r * Hq + (size_t)kvh * G) * D;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int e = 0; e < E2; ++e) {
-          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qg + h * D + lane * E + 2 * e));
-          q2[h][e] = f32x2_mul(bf16x2_to_f32x2(w), sc2);
-          acc2[h][e] = 0ull;
-        }
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qg + g * D + 16 * ks + 2 * t)) : 0u;
+        qa[ks][2] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qg + g * D + 16 * ks + 8 + 2 * t)) : 0u;
+        qa[ks][1] = qa[ks][3] = 0u;
       }
-      m_l = -INFINITY;
-      l_l = 0.f;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+      m_r = -INFINITY;
+      l_r = 0.f;
     }
-    const __nv_bfloat16* ks =
-        reinterpret_cast<const __nv_bfloat16*>(smem + (size_t)stage * 2 * Cfg::TILE_BYTES) + warp * D + lane * E;
-    const __nv_bfloat16* vs = ks + Cfg::TILE_BYTES / 2;
-#pragma unroll 1
-    for (int grp = 0; grp < Cfg::GROUPS; ++grp) {
-      const int tb = grp * TG;
-      if (tb >= inf.n) break;
-      float vals[32];
+    if (inf.n > 0) {
+      const uint32_t ks_base = sbase + stage * 2 * Cfg::TILE + warp * D * 2;  // this head's K rows
+      const uint32_t vs_base = ks_base + Cfg::TILE;
+      // ---- S[16 x 16 tokens] = Q K^T: n-blocks of tokens 0..7 and 8..15
+      float sacc[2][4];
 #pragma unroll
-      for (int t = 0; t < TG; ++t) {
-        uint64_t k2[E2];
-        const __nv_bfloat16* kp = ks + (size_t)(tb + t) * HB * D;
-        if constexpr (E == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(kp);
-          k2[0] = bf16x2_to_f32x2(w.x);
-          k2[1] = bf16x2_to_f32x2(w.y);
-        } else {
-          k2[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(kp));
-        }
+      for (int nb = 0; nb < 2; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          uint64_t x2 = f32x2_mul(q2[h][0], k2[0]);
-#pragma unroll
-          for (int e = 1; e < E2; ++e) x2 = f32x2_fma(q2[h][e], k2[e], x2);
-          float xl, xh;
-          f32x2_unpack(x2, xl, xh);
-          vals[h * TG + t] = xl + xh;
-        }
+      for (int ks = 0; ks < KS; ++ks) {
+        // matrices: (tokens 0..7, dims 16ks..), (0..7, 16ks + 8..), (8..15, 16ks..), (8..15, 16ks + 8..)
+        uint32_t b[4];
+        const int row = (lane & 7) + ((lane >> 4) << 3);
+        ldsm_x4(ks_base + row * Cfg::ROW + (16 * ks + ((lane >> 3) & 1) * 8) * 2, b);
+        mma_16816(sacc[0], qa[ks], b[0], b[1]);
+        mma_16816(sacc[1], qa[ks], b[2], b[3]);
       }
-      // 32-way reduce-scatter: afterwards lane holds the full score of value `lane`.
+      // ---- online softmax of row g (rows g + 8 hold no query head: their P stays zero)
+      float sv[4];
 #pragma unroll
-      for (int k = 16; k >= 1; k >>= 1) {
-        const bool upper = (lane & k) != 0;
-#pragma unroll
-        for (int i = 0; i < k; ++i) {
-          const float send = upper ? vals[i] : vals[i + k];
-          const float keep = upper ? vals[i + k] : vals[i];
-          vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
-        }
+      for (int nb = 0; nb < 2; ++nb) {
+        const int j = 8 * nb + 2 * t;
+        sv[2 * nb] = j < inf.n ? sacc[nb][0] * A.scale_log2 : -INFINITY;
+        sv[2 * nb + 1] = j + 1 < inf.n ? sacc[nb][1] * A.scale_log2 : -INFINITY;
       }
-      const bool valid = tb + my_t < inf.n;
-      const float s = valid ? vals[0] : -INFINITY;
-      float mx = s;
+      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      // every tile holds at least one valid token, so the new maximum is finite
+      const float mn = fmaxf(m_r, mx);
+      const float al = exp2f(m_r - mn);  // m_r = -inf -> 0
+      m_r = mn;
+      float p[4];
 #pragma unroll
-      for (int o = TG / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float m_new = fmaxf(m_l, mx);
-      const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_l - m_new);
-      const float p = valid ? exp2f(s - m_new) : 0.f;
-      float ps = p;
+      for (int i = 0; i < 4; ++i) p[i] = exp2f(sv[i] - mn);
+      l_r = l_r * al + ((p[0] + p[1]) + (p[2] + p[3]));
 #pragma unroll
-      for (int o = TG / 2; o >= 1; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-      l_l = l_l * alpha + ps;
-      m_l = m_new;
-      s_p[warp][my_t * G + my_h] = p;
-      if (my_t == 0) s_alpha[warp][my_h] = alpha;
-      __syncwarp();
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float a_h = s_alpha[warp][h];
-        const uint64_t a2 = f32x2_pack(a_h, a_h);
-#pragma unroll
-        for (int e = 0; e < E2; ++e) acc2[h][e] = f32x2_mul(acc2[h][e], a2);
+      for (int i = 0; i < NB; ++i) {
+        oacc[i][0] *= al;
+        oacc[i][1] *= al;
       }
-      const int nv = min(TG, inf.n - tb);
-#pragma unroll 4
-      for (int t = 0; t < nv; ++t) {
-        float pv[G];
+      // P as the A operand of one k-step over the 16 tokens (the accumulator layout of two
+      // adjacent n-blocks is the A fragment layout); rows g + 8 are zero
+      const uint32_t pa[4] = {pack_bf16x2(p[0], p[1]), 0u, pack_bf16x2(p[2], p[3]), 0u};
+      // ---- O[16 x D] += P V
 #pragma unroll
-        for (int h = 0; h < G; ++h) pv[h] = s_p[warp][t * G + h];
-        uint64_t v2[E2];
-        const __nv_bfloat16* vp = vs + (size_t)(tb + t) * HB * D;
-        if constexpr (E == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(vp);
-          v2[0] = bf16x2_to_f32x2(w.x);
-          v2[1] = bf16x2_to_f32x2(w.y);
-        } else {
-          v2[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(vp));
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const uint64_t p2 = f32x2_pack(pv[h], pv[h]);
-#pragma unroll
-          for (int e = 0; e < E2; ++e) acc2[h][e] = f32x2_fma(p2, v2[e], acc2[h][e]);
-        }
+      for (int nbd = 0; nbd < NB; nbd += 2) {
+        // matrices (transposed): (tokens 0..7, dims 8nbd..), (8..15, 8nbd..), (0..7, 8nbd + 8..), (8..15, 8nbd + 8..)
+        uint32_t b[4];
+        const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
+        ldsm_x4_t(vs_base + row * Cfg::ROW + (8 * nbd + ((lane >> 4) << 3)) * 2, b);
+        mma_16816(oacc[nbd], pa, b[0], b[1]);
+        mma_16816(oacc[nbd + 1], pa, b[2], b[3]);
       }
-      __syncwarp();
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[stage]);
     if (++stage == STAGES) { stage = 0; ++round; }
 
     if (inf.flags & kLast) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float l_h = __shfl_sync(0xffffffffu, l_l, h * TG);
-        const float m_h = __shfl_sync(0xffffffffu, m_l, h * TG);
-        const float inv = l_h > 0.f ? 1.f / l_h : 0.f;
-        const float lse_h = l_h > 0.f ? (m_h + log2f(l_h)) * kLn2 : -INFINITY;
-        const size_t row = (size_t)g * G + h;
-        float acc[E];
-#pragma unroll
-        for (int e = 0; e < E2; ++e) f32x2_unpack(acc2[h][e], acc[2 * e], acc[2 * e + 1]);
+      float lr = l_r;  // row g: the quad's shares
+      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+      if (g < G) {
+        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float lse_h = lr > 0.f ? (m_r + log2f(lr)) * kLn2 : -INFINITY;
+        const size_t row = (size_t)kvh * G + g;
         if (inf.flags & kFinal) {
-          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + ((size_t)inf.r * Hq + row) * D + lane * E;
+          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + ((size_t)inf.r * Hq + row) * D + 2 * t;
 #pragma unroll
-          for (int e = 0; e < E; e += 2)
-            *reinterpret_cast<__nv_bfloat162*>(op + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-          if (A.lse && lane == 0) A.lse[(size_t)inf.r * Hq + row] = lse_h;
+          for (int i = 0; i < NB; ++i)
+            *reinterpret_cast<uint32_t*>(op + 8 * i) = pack_bf16x2(oacc[i][0] * inv, oacc[i][1] * inv);
+          if (A.lse && t == 0) A.lse[(size_t)inf.r * Hq + row] = lse_h;
         } else {
-          float* op = A.part_o + ((size_t)inf.slot * Hq + row) * D + lane * E;
+          float* op = A.part_o + ((size_t)inf.slot * Hq + row) * D + 2 * t;
 #pragma unroll
-          for (int e = 0; e < E; ++e) op[e] = acc[e] * inv;
-          if (lane == 0) A.part_lse[(size_t)inf.slot * Hq + row] = lse_h;
+          for (int i = 0; i < NB; ++i) *reinterpret_cast<float2*>(op + 8 * i) = make_float2(oacc[i][0] * inv, oacc[i][1] * inv);
+          if (t == 0) A.part_lse[(size_t)inf.slot * Hq + row] = lse_h;
         }
       }
     }
@@ -454,7 +412,7 @@ sta_status plan_t(DecodeArgs& a, int64_t T, int device) {
   const int64_t per_x = ctas / (a.Hkv / HB) > 0 ? ctas / (a.Hkv / HB) : 1;  // CTAs along the token axis
   if (a.mode == 0) {
     int64_t rl = T > 0 ? cdiv(T, per_x) : 1;
-    if (rl < Cfg::NT) rl = Cfg::NT;
+    if (rl < kNT) rl = kNT;
     a.range_len = (int)rl;
     a.n_ranges = (int)(T > 0 ? cdiv(T, rl) : 0);
   } else {
@@ -487,11 +445,10 @@ int pick_hb(int Hkv) {
 template <int G, int D>
 sta_status dispatch_hb(DecodeArgs& a, int64_t T, int device, cudaStream_t st, bool plan) {
   int hb = pick_hb(a.Hkv);
-  constexpr bool kWide = (G == 1 && D == 128);  // 32-token tiles: at most 4 heads per CTA fit
-  if (kWide && hb > 4) hb = 4;
+  if (D == 128 && hb > 4) hb = 4;  // at d = 128 a CTA serves at most 4 heads (two CTAs per SM)
   switch (hb) {
     case 8:
-      if constexpr (!kWide) return plan ? plan_t<G, D, 8>(a, T, device) : launch_t<G, D, 8>(a, st);
+      if constexpr (D == 64) return plan ? plan_t<G, D, 8>(a, T, device) : launch_t<G, D, 8>(a, st);
       return STA_ERR_UNSUPPORTED;
     case 4: return plan ? plan_t<G, D, 4>(a, T, device) : launch_t<G, D, 4>(a, st);
     case 2: return plan ? plan_t<G, D, 2>(a, T, device) : launch_t<G, D, 2>(a, st);
