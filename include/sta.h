@@ -434,7 +434,8 @@ sta_status sta_decode_splitkv_noalloc(const void* q, const void* k, const void* 
 /* sta_merge_lse -- merge s partial attention results per row:
  *   M = max_i lse_i; if M = -inf then O = 0, LSE = -inf; otherwise
  *   w_i = exp(lse_i - M), O = sum_i w_i O_i / sum_i w_i, LSE = M + log sum_i w_i.
- *   part_o   [n_rows, s, d] float32 normalised partial outputs (device)
+ *   part_o   [n_rows, s, d] float32 normalised partial outputs (device, 16-byte
+ *            aligned, else STA_ERR_UNSUPPORTED)
  *   part_lse [n_rows, s]    float32 natural-log partial denominators (device)
  *   o        [n_rows, d]    o_dtype (device, written); lse [n_rows] f32 or NULL
  *   1 <= s <= 4096; d in {32, 64, 128, 256}; n_rows == 0 is a no-op.

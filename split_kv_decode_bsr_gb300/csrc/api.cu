@@ -419,5 +419,6 @@ extern "C" sta_status sta_merge_lse(const float* part_o, const float* part_lse, 
   if (d != 32 && d != 64 && d != 128 && d != 256) return STA_ERR_UNSUPPORTED;
   if (n_rows == 0) return STA_OK;
   if (!part_o || !part_lse || !o) return STA_ERR_INVALID_ARG;
+  if ((uintptr_t)part_o & 15u) return STA_ERR_UNSUPPORTED;  // partials are read 16 bytes at a time
   return launch_merge_public(part_o, part_lse, n_rows, s, d, o, o_dtype, lse, (cudaStream_t)stream);
 }

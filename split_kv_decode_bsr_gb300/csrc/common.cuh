@@ -63,23 +63,70 @@ __device__ __forceinline__ uint64_t part_row_bits(const uint64_t* words, int r) 
 
 // Merge s partials of one row; lane owns E consecutive dims. po points at the
 // row's first partial, consecutive partials `ostride` floats apart; lse values
-// `lstride` apart. Writes out[E] and returns the merged LSE.
+// `lstride` apart. Writes out[E] and returns the merged LSE. The partials are
+// added in order 0..s-1. The first 32 LSEs (one per lane) and the first U
+// partials' values are loaded together, before the maximum is known, and later
+// partials U at a time, so that a row costs about one memory round trip per U
+// partials instead of one per partial.
+template <int E>
+__device__ __forceinline__ void load_dims(const float* p, float* v) {
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(p) + q);
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+  } else if constexpr (E % 2 == 0) {
+#pragma unroll
+    for (int q = 0; q < E / 2; ++q) {
+      const float2 x = __ldg(reinterpret_cast<const float2*>(p) + q);
+      v[2 * q] = x.x; v[2 * q + 1] = x.y;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = __ldg(p + e);
+  }
+}
+
 template <int E>
 __device__ __forceinline__ float merge_row(const float* po, size_t ostride, const float* pl, size_t lstride, int s,
                                            int lane, float* out) {
-  float M = -INFINITY;
-  for (int i = lane; i < s; i += 32) M = fmaxf(M, __ldg(pl + (size_t)i * lstride));
+  constexpr int U = E >= 8 ? 2 : 4;  // partials in flight per lane
+  const float lse_l = lane < s ? __ldg(pl + (size_t)lane * lstride) : -INFINITY;
+  float v[U][E];
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (u < s) load_dims<E>(po + (size_t)u * ostride + lane * E, v[u]);
+  float M = lse_l;
+  for (int i = lane + 32; i < s; i += 32) M = fmaxf(M, __ldg(pl + (size_t)i * lstride));
   M = warp_max(M);
 #pragma unroll
   for (int e = 0; e < E; ++e) out[e] = 0.f;
   if (M == -INFINITY) return -INFINITY;
   float wsum = 0.f;
-  for (int i = 0; i < s; ++i) {
-    const float w = exp2f((__ldg(pl + (size_t)i * lstride) - M) * kLog2e);
-    wsum += w;
-    const float* p = po + (size_t)i * ostride + lane * E;
+  for (int i0 = 0; i0 < s; i0 += 32) {
+    const int nb = min(32, s - i0);
+    // lane j: the weight of partial i0 + j
+    const float x = i0 == 0 ? lse_l : (lane < nb ? __ldg(pl + (size_t)(i0 + lane) * lstride) : -INFINITY);
+    const float wl = lane < nb ? exp2f((x - M) * kLog2e) : 0.f;
+    for (int j = 0; j < nb; j += U) {
+      if (i0 + j > 0) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = fmaf(w, __ldg(p + e), out[e]);
+        for (int u = 0; u < U; ++u)
+          if (j + u < nb) load_dims<E>(po + (size_t)(i0 + j + u) * ostride + lane * E, v[u]);
+      }
+      float w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) w[u] = __shfl_sync(0xffffffffu, wl, min(j + u, 31));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (j + u < nb) {
+          wsum += w[u];
+#pragma unroll
+          for (int e = 0; e < E; ++e) out[e] = fmaf(w[u], v[u][e], out[e]);
+        }
+      }
+    }
   }
   const float inv = 1.f / wsum;
 #pragma unroll

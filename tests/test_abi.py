@@ -139,6 +139,8 @@ def test_merge_rejects_bad_arguments_on_host(lib):
     assert lib.sta_merge_lse(P, P, 4, 2, 64, P, 7, None, None) == sta.STA_ERR_INVALID_ARG
     assert lib.sta_merge_lse(None, P, 4, 2, 64, P, 0, None, None) == sta.STA_ERR_INVALID_ARG
     assert lib.sta_merge_lse(None, None, 0, 2, 64, None, 0, None, None) == sta.STA_OK
+    # partials are read 16 bytes at a time: a pointer off that boundary is refused before any launch
+    assert lib.sta_merge_lse(C.c_void_p(256 + 4), P, 4, 2, 64, P, 0, None, None) == sta.STA_ERR_UNSUPPORTED
 
 
 def _mha_split(lib, splits, B=1, H=2, Lq=128, d=64, ws=None, ws_bytes=0, kernel=0, dtype=sta.STA_BF16):
