@@ -104,25 +104,6 @@ struct PageCache {
   }
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// D += A (16 x 16, row) * B (16 x 8, col); bf16 operands, fp32 accumulators
-__device__ __forceinline__ void mma_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 template <int G, int D, int HB>
 __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(const DecodeArgs A) {
   using Cfg = DecCfg<G, D, HB>;
@@ -266,8 +247,8 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(co
         uint32_t b[4];
         const int row = (lane & 7) + ((lane >> 4) << 3);
         ldsm_x4(ks_base + row * Cfg::ROW + (16 * ks + ((lane >> 3) & 1) * 8) * 2, b);
-        mma_16816(sacc[0], qa[ks], b[0], b[1]);
-        mma_16816(sacc[1], qa[ks], b[2], b[3]);
+        mma_bf16_16816(sacc[0], qa[ks], b[0], b[1]);
+        mma_bf16_16816(sacc[1], qa[ks], b[2], b[3]);
       }
       // ---- online softmax of row g (rows g + 8 hold no query head: their P stays zero)
       float sv[4];
@@ -303,8 +284,8 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(co
         uint32_t b[4];
         const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
         ldsm_x4_t(vs_base + row * Cfg::ROW + (8 * nbd + ((lane >> 4) << 3)) * 2, b);
-        mma_16816(oacc[nbd], pa, b[0], b[1]);
-        mma_16816(oacc[nbd + 1], pa, b[2], b[3]);
+        mma_bf16_16816(oacc[nbd], pa, b[0], b[1]);
+        mma_bf16_16816(oacc[nbd + 1], pa, b[2], b[3]);
       }
     }
     __syncwarp();

@@ -70,25 +70,6 @@ struct MlaArgs {
   int* err;
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// D += A (16 x 16, row) * B (16 x 8, col); bf16 operands, fp32 accumulators
-__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Request r's token range from the device indptr, kept inside [0, T] and non-decreasing.
 __device__ __forceinline__ void mla_range(const MlaArgs& A, int r, int& rb, int& re) {
   rb = __ldg(A.kv_indptr + r);
@@ -269,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 2) mla_decode_kernel(const MlaArgs A
       for (int i = 0; i < kKhalf; ++i) {
         uint32_t b[4];
         ldsm_x4(k_addr + i * 32, b);
-        mma_bf16(sacc[i & 1][0], qa[i], b[0], b[1]);
-        mma_bf16(sacc[i & 1][1], qa[i], b[2], b[3]);
+        mma_bf16_16816(sacc[i & 1][0], qa[i], b[0], b[1]);
+        mma_bf16_16816(sacc[i & 1][1], qa[i], b[2], b[3]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&kv_empty[s]);  // the rows' keys are read
@@ -397,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 2) mla_decode_kernel(const MlaArgs A
     for (int nbd = 0; nbd < kNbDv; nbd += 2) {
       uint32_t b[4];
       ldsm_x4_t(vs + nbd * 16, b);
-      mma_bf16(oacc[nbd], pa, b[0], b[1]);
-      mma_bf16(oacc[nbd + 1], pa, b[2], b[3]);
+      mma_bf16_16816(oacc[nbd], pa, b[0], b[1]);
+      mma_bf16_16816(oacc[nbd + 1], pa, b[2], b[3]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&kv_empty[s]);
