@@ -261,6 +261,33 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
       // gives wrong values but no read outside K and V
       base = (int64_t)min((unsigned)__ldg(A.mask.part_col_idx + tt), (unsigned)A.mask.ot_cols - 1u) * 64;
     }
+    // all keys of the round at once when they fit the list: each lane writes its tile's keys
+    // at the prefix of the lanes below it (the same ascending order as one tile at a time)
+    const int cnt = __popcll(bits);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (nk + total <= 72) {
+      int pos = nk + incl - cnt;
+      for (uint64_t bm = bits; bm; bm &= bm - 1) keys[pos++] = (int)min(base + (__ffsll(bm) - 1), (int64_t)A.Lk - 1);
+      nk += total;
+      __syncwarp();
+      if (nk >= NB) {
+        int b0 = 0;
+        for (; nk - b0 >= NB; b0 += NB) batch(b0, NB);
+        const int left = nk - b0;
+        const int kl = lane < left ? keys[b0 + lane] : 0;
+        __syncwarp();
+        if (lane < left) keys[lane] = kl;
+        nk = left;
+        __syncwarp();
+      }
+      continue;
+    }
     for (unsigned nz = __ballot_sync(0xffffffffu, bits != 0ull); nz; nz &= nz - 1) {
       const int src = __ffs(nz) - 1;
       const uint64_t mb64 = __shfl_sync(0xffffffffu, bits, src);
