@@ -414,9 +414,9 @@ sta_status sta_decode_splitkv_paged(const void* q, const void* k_pages, const vo
  * fit it: slots * Hq * (d + 1) * 4 bytes (each part rounded up to 256) <= 16 MiB.
  * With num_splits > 0, slots = n_req * num_splits. With num_splits == 0, slots =
  * ranges + n_req, where ranges (the token ranges the plan cuts the KV stream
- * into) is at most ceil(T / 8) and at most the resident decode CTAs divided by
- * the KV-head groups a CTA serves; the sum resident CTAs + n_req is therefore an
- * upper bound, not the exact size. Query the exact size with sta_decode_splitkv
+ * into, each at least 16 tokens) is at most ceil(T / 16) and at most the
+ * resident decode CTAs divided by the KV-head groups a CTA serves; the sum
+ * resident CTAs + n_req is therefore an upper bound, not the exact size. Query the exact size with sta_decode_splitkv
  * (workspace == NULL). A larger plan returns STA_ERR_WORKSPACE and launches
  * nothing.
  * The first call on each device looks up the array's device address (with that
