@@ -358,7 +358,7 @@ int sta_mha_select_kernel(const sta_bsr_mask* mask, int B, int H, int Lq, int Lk
  *                  kv_indptr[r] .. kv_indptr[r+1]-1; may be NULL when T == 0
  *                  (every request then gets O = 0, LSE = -inf)
  *   kv_indptr_dev  int32 [n_req+1] (device), kv_indptr_host: same values (host)
- *   Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8}, d in {64, 128}
+ *   Hq % Hkv == 0, Hq / Hkv in {1, 2, 4, 8, 16}, d in {64, 128}
  *   num_splits     0: the library picks the split (the whole token stream is
  *                  cut into equal ranges, one per resident CTA); s > 0: every
  *                  request is cut into s chunks of ceil(len/s) keys

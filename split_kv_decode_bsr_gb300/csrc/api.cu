@@ -327,7 +327,7 @@ sta_status decode_setup(const int32_t* indptr_host, int n_req, int Hq, int Hkv, 
     return STA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return STA_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return STA_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return STA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return STA_ERR_UNSUPPORTED;
   if (dtype != STA_BF16) return STA_ERR_UNSUPPORTED;
   if (indptr_host[0] != 0) return STA_ERR_INVALID_ARG;

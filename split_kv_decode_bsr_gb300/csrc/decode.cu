@@ -7,8 +7,8 @@
 // heads x d, bf16) from HBM into a ring of shared-memory stages with 1-D bulk copies, one per
 // token row, completing on mbarriers; packed and paged K/V differ only in where a row is read
 // from. HB consumer warps (one per kv head) compute on the tensor cores with
-// mma.sync.m16n8k16 (bf16 operands, fp32 accumulators): the warp's G query heads are the M of
-// the MMA (rows G..15 are zero), S[16 x 16 tokens] = Q K^T takes d / 16 k-steps over K rows
+// mma.sync.m16n8k16 (bf16 operands, fp32 accumulators): the warp's G <= 16 query heads are the
+// M of the MMA (rows G..15 are zero), S[16 x 16 tokens] = Q K^T takes d / 16 k-steps over K rows
 // read by ldmatrix, the fp32 online softmax runs on the accumulator fragments (a quad of
 // lanes holds a row), P passes from the S fragments straight into the A fragments of P V, and
 // O[16 x d] accumulates in registers over V rows read by ldmatrix .trans. Token rows are
@@ -211,9 +211,11 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(co
   const int kvh = g0 + warp;              // kv head of this warp
   const int Hq = A.Hq;
   const uint32_t sbase = smem_u32(smem);
+  // fragment rows of this lane that hold query heads: g, and g + 8 when G = 16
+  constexpr int NR = G > 8 ? 2 : 1;
   uint32_t qa[KS][4];
   float oacc[NB][4];
-  float m_r = -INFINITY, l_r = 0.f;  // running max of row g, this lane's share of its sum
+  float m_r[NR], l_r[NR];  // running max of each row, this lane's share of its sum
   int stage = 0;
   uint32_t round = 0;
   for (;;) {
@@ -221,18 +223,26 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(co
     const StageInfo inf = info[stage];
     if (inf.flags & kDone) break;
     if (inf.flags & kFirst) {
-      // query rows of this warp's G heads as mma A fragments (row g: head g; rows >= G zero)
+      // query rows of this warp's G heads as mma A fragments (row x: head x; rows >= G zero)
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(A.q) + ((size_t)inf.r * Hq + (size_t)kvh * G) * D;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         qa[ks][0] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qg + g * D + 16 * ks + 2 * t)) : 0u;
         qa[ks][2] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(qg + g * D + 16 * ks + 8 + 2 * t)) : 0u;
-        qa[ks][1] = qa[ks][3] = 0u;
+        if constexpr (NR == 2) {
+          qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qg + (g + 8) * D + 16 * ks + 2 * t));
+          qa[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(qg + (g + 8) * D + 16 * ks + 8 + 2 * t));
+        } else {
+          qa[ks][1] = qa[ks][3] = 0u;
+        }
       }
 #pragma unroll
       for (int i = 0; i < NB; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-      m_r = -INFINITY;
-      l_r = 0.f;
+#pragma unroll
+      for (int rr = 0; rr < NR; ++rr) {
+        m_r[rr] = -INFINITY;
+        l_r[rr] = 0.f;
+      }
     }
     if (inf.n > 0) {
       const uint32_t ks_base = sbase + stage * 2 * Cfg::TILE + warp * D * 2;  // this head's K rows
@@ -250,33 +260,49 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(co
         mma_bf16_16816(sacc[0], qa[ks], b[0], b[1]);
         mma_bf16_16816(sacc[1], qa[ks], b[2], b[3]);
       }
-      // ---- online softmax of row g (rows g + 8 hold no query head: their P stays zero)
-      float sv[4];
+      // ---- online softmax of row g (and of row g + 8 when it holds a query head; else its P
+      // stays zero)
+      float p[NR][4], al[NR];
 #pragma unroll
-      for (int nb = 0; nb < 2; ++nb) {
-        const int j = 8 * nb + 2 * t;
-        sv[2 * nb] = j < inf.n ? sacc[nb][0] * A.scale_log2 : -INFINITY;
-        sv[2 * nb + 1] = j + 1 < inf.n ? sacc[nb][1] * A.scale_log2 : -INFINITY;
+      for (int rr = 0; rr < NR; ++rr) {
+        float sv[4];
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          const int j = 8 * nb + 2 * t;
+          sv[2 * nb] = j < inf.n ? sacc[nb][2 * rr] * A.scale_log2 : -INFINITY;
+          sv[2 * nb + 1] = j + 1 < inf.n ? sacc[nb][2 * rr + 1] * A.scale_log2 : -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // every tile holds at least one valid token, so the new maximum is finite
+        const float mn = fmaxf(m_r[rr], mx);
+        al[rr] = exp2f(m_r[rr] - mn);  // m = -inf -> 0
+        m_r[rr] = mn;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[rr][i] = exp2f(sv[i] - mn);
+        l_r[rr] = l_r[rr] * al[rr] + ((p[rr][0] + p[rr][1]) + (p[rr][2] + p[rr][3]));
       }
-      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      // every tile holds at least one valid token, so the new maximum is finite
-      const float mn = fmaxf(m_r, mx);
-      const float al = exp2f(m_r - mn);  // m_r = -inf -> 0
-      m_r = mn;
-      float p[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) p[i] = exp2f(sv[i] - mn);
-      l_r = l_r * al + ((p[0] + p[1]) + (p[2] + p[3]));
 #pragma unroll
       for (int i = 0; i < NB; ++i) {
-        oacc[i][0] *= al;
-        oacc[i][1] *= al;
+        oacc[i][0] *= al[0];
+        oacc[i][1] *= al[0];
+        if constexpr (NR == 2) {
+          oacc[i][2] *= al[NR - 1];
+          oacc[i][3] *= al[NR - 1];
+        }
       }
       // P as the A operand of one k-step over the 16 tokens (the accumulator layout of two
-      // adjacent n-blocks is the A fragment layout); rows g + 8 are zero
-      const uint32_t pa[4] = {pack_bf16x2(p[0], p[1]), 0u, pack_bf16x2(p[2], p[3]), 0u};
+      // adjacent n-blocks is the A fragment layout); rows g + 8 are zero unless they hold heads
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
+      pa[2] = pack_bf16x2(p[0][2], p[0][3]);
+      if constexpr (NR == 2) {
+        pa[1] = pack_bf16x2(p[NR - 1][0], p[NR - 1][1]);
+        pa[3] = pack_bf16x2(p[NR - 1][2], p[NR - 1][3]);
+      } else {
+        pa[1] = pa[3] = 0u;
+      }
       // ---- O[16 x D] += P V
 #pragma unroll
       for (int nbd = 0; nbd < NB; nbd += 2) {
@@ -293,24 +319,29 @@ __global__ void __launch_bounds__(DecCfg<G, D, HB>::THREADS, 2) decode_kernel(co
     if (++stage == STAGES) { stage = 0; ++round; }
 
     if (inf.flags & kLast) {
-      float lr = l_r;  // row g: the quad's shares
-      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
-      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
-      if (g < G) {
-        const float inv = lr > 0.f ? 1.f / lr : 0.f;
-        const float lse_h = lr > 0.f ? (m_r + log2f(lr)) * kLn2 : -INFINITY;
-        const size_t row = (size_t)kvh * G + g;
-        if (inf.flags & kFinal) {
-          __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + ((size_t)inf.r * Hq + row) * D + 2 * t;
 #pragma unroll
-          for (int i = 0; i < NB; ++i)
-            *reinterpret_cast<uint32_t*>(op + 8 * i) = pack_bf16x2(oacc[i][0] * inv, oacc[i][1] * inv);
-          if (A.lse && t == 0) A.lse[(size_t)inf.r * Hq + row] = lse_h;
-        } else {
-          float* op = A.part_o + ((size_t)inf.slot * Hq + row) * D + 2 * t;
+      for (int rr = 0; rr < NR; ++rr) {
+        float lr = l_r[rr];  // the quad's shares
+        lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+        lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+        const int x = g + 8 * rr;  // query head of this fragment row within the group
+        if (x < G) {
+          const float inv = lr > 0.f ? 1.f / lr : 0.f;
+          const float lse_h = lr > 0.f ? (m_r[rr] + log2f(lr)) * kLn2 : -INFINITY;
+          const size_t row = (size_t)kvh * G + x;
+          if (inf.flags & kFinal) {
+            __nv_bfloat16* op = static_cast<__nv_bfloat16*>(A.o) + ((size_t)inf.r * Hq + row) * D + 2 * t;
 #pragma unroll
-          for (int i = 0; i < NB; ++i) *reinterpret_cast<float2*>(op + 8 * i) = make_float2(oacc[i][0] * inv, oacc[i][1] * inv);
-          if (t == 0) A.part_lse[(size_t)inf.slot * Hq + row] = lse_h;
+            for (int i = 0; i < NB; ++i)
+              *reinterpret_cast<uint32_t*>(op + 8 * i) = pack_bf16x2(oacc[i][2 * rr] * inv, oacc[i][2 * rr + 1] * inv);
+            if (A.lse && t == 0) A.lse[(size_t)inf.r * Hq + row] = lse_h;
+          } else {
+            float* op = A.part_o + ((size_t)inf.slot * Hq + row) * D + 2 * t;
+#pragma unroll
+            for (int i = 0; i < NB; ++i)
+              *reinterpret_cast<float2*>(op + 8 * i) = make_float2(oacc[i][2 * rr] * inv, oacc[i][2 * rr + 1] * inv);
+            if (t == 0) A.part_lse[(size_t)inf.slot * Hq + row] = lse_h;
+          }
         }
       }
     }
@@ -444,6 +475,7 @@ sta_status dispatch_g(DecodeArgs& a, int64_t T, int device, cudaStream_t st, boo
     case 2: return dispatch_hb<2, D>(a, T, device, st, plan);
     case 4: return dispatch_hb<4, D>(a, T, device, st, plan);
     case 8: return dispatch_hb<8, D>(a, T, device, st, plan);
+    case 16: return dispatch_hb<16, D>(a, T, device, st, plan);
     default: return STA_ERR_UNSUPPORTED;
   }
 }

@@ -123,6 +123,7 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     good = [0, 5, 9]
     assert _dec(lib, good, 2, Hq=12, Hkv=8) == sta.STA_ERR_INVALID_ARG  # Hq % Hkv
     assert _dec(lib, good, 2, Hq=24, Hkv=8) == sta.STA_ERR_UNSUPPORTED  # group of 3
+    assert _dec(lib, good, 2, Hq=64, Hkv=2) == sta.STA_ERR_UNSUPPORTED  # group of 32 (at most 16 heads per KV head)
     assert _dec(lib, good, 2, d=96) == sta.STA_ERR_UNSUPPORTED
     assert _dec(lib, good, 2, dtype=sta.STA_F32) == sta.STA_ERR_UNSUPPORTED
     assert _dec(lib, [0, 5, 3], 2) == sta.STA_ERR_INVALID_ARG  # non-monotone kv_indptr

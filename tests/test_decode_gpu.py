@@ -34,7 +34,8 @@ def _run(wl, dev, num_splits, o_ref=None, lse_ref=None):
 
 
 @pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 2, 64), (8, 8, 128), (16, 8, 64), (16, 2, 128),
-                                      (8, 1, 64), (4, 4, 64), (24, 24, 128), (64, 8, 128)])
+                                      (8, 1, 64), (4, 4, 64), (24, 24, 128), (64, 8, 128),
+                                      (128, 8, 128), (32, 2, 64), (16, 1, 128)])
 @pytest.mark.parametrize("num_splits", [0, 1, 2, 3, 7])
 def test_ragged_small(dev, Hq, Hkv, d, num_splits):
     lens = [0, 1, 7, 8, 9, 64, 100, 1000, 3, 2500]

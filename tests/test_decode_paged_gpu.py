@@ -43,7 +43,7 @@ def _both(wl, page_size, dev, num_splits, seed=1):
     return o_p, lse_p
 
 
-@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 2, 64), (24, 24, 128), (16, 2, 128)])
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (8, 2, 64), (24, 24, 128), (16, 2, 128), (128, 8, 128)])
 @pytest.mark.parametrize("page_size", [1, 8, 16, 100])
 @pytest.mark.parametrize("num_splits", [0, 3])
 def test_paged_equals_contiguous_and_oracle(dev, Hq, Hkv, d, page_size, num_splits):
