@@ -43,6 +43,14 @@ def test_ragged_small(dev, Hq, Hkv, d, num_splits):
     _run(wl, dev, num_splits)
 
 
+@pytest.mark.parametrize("num_splits", [0, 5])
+def test_one_long_request(dev, num_splits):
+    # a single 100,000-token request: the library's plan spreads it over every resident CTA's
+    # range, so each output row merges one partial per range
+    wl = W.gqa_decode(seed=9, n_req=1, Hq=32, Hkv=8, d=128, lengths=[100000])
+    _run(wl, dev, num_splits)
+
+
 def test_all_empty_requests(dev):
     wl = W.gqa_decode(seed=4, n_req=3, Hq=8, Hkv=2, d=64, lengths=[0, 0, 0])
     _run(wl, dev, 0)

@@ -52,6 +52,27 @@ def test_head_groups(dev, Hq):
     _run(dev, wl, chunk_tokens=128)
 
 
+def test_all_requests_empty(dev):
+    # no cached row at all (T = 0): every row O = 0 and LSE = -inf
+    wl = W.mla_decode(seed=6, n_req=3, lengths=[0, 0, 0])
+    _run(dev, wl)
+    _run(dev, wl, chunk_tokens=32)
+
+
+def test_one_long_request_cut_into_many_chunks(dev):
+    # a single 40,000-token request: the library's plan cuts it into 250 chunks of 160 tokens
+    # (one wave of CTAs), all merged into one row per head
+    wl = W.mla_decode(seed=7, n_req=1, lengths=[40000])
+    _run(dev, wl)
+
+
+def test_most_query_heads(dev):
+    # Hq = 1024: 64 head groups along the grid's y axis
+    wl = W.mla_decode(seed=8, n_req=2, Hq=1024, lengths=[3, 40])
+    _run(dev, wl)
+    _run(dev, wl, chunk_tokens=32)
+
+
 def test_wide_score_range(dev):
     # large scale: the running maximum moves often inside and across tiles and chunks
     wl = W.mla_decode(seed=5, n_req=2, lengths=[900, 2000], scale=0.5)
