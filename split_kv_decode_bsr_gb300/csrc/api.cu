@@ -46,13 +46,13 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // The ratio is the measured crossover on GB300. Unstructured masks over B=1, H=8, L=4096
 // (every outer tile part; time in us, row / block):
 //   density   0.1 %      0.2 %      0.4 %      1 %         2 %         5 %
-//   d = 64    52 / 82    58 / 82    64 / 82    89 / 82     128 / 82    353 / 81
-//   d = 128   55 / 80    60 / 80    73 / 81    109 / 80    169 / 80    460 / 80
+//   d = 64    38 / 82    44 / 83    54 / 82    79 / 83     120 / 82    353 / 82
+//   d = 128   44 / 80    50 / 80    62 / 80    99 / 80     158 / 80    444 / 80
 // The block kernel's time does not follow the fill of its tiles (part tiles are bound by
 // the softmax at both head sizes), the row kernel's follows the valid pairs; the two meet
-// near 0.85 % density at d = 64 and 0.53 % at d = 128, i.e. the row kernel spends ~118x
-// (d = 64) and ~189x (d = 128) the block kernel's time per computed pair on each valid pair.
-double row_over_block(int d) { return d == 64 ? 118.0 : 189.0; }
+// near 1.09 % density at d = 64 and 0.70 % at d = 128, i.e. the row kernel spends ~92x
+// (d = 64) and ~143x (d = 128) the block kernel's time per computed pair on each valid pair.
+double row_over_block(int d) { return d == 64 ? 92.0 : 143.0; }
 constexpr int kMaxSplitsPrefill = 1024;
 
 int choose(int64_t tiles, int64_t valid, int d) {

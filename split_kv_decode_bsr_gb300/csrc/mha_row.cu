@@ -103,9 +103,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   constexpr int E = D / 32;
   __shared__ __align__(16) float s_q[kRowWarps][D];
   __shared__ int s_keys[kRowWarps][72];  // valid keys waiting for a batch: fewer than 8, plus one tile's 64
+  // a scan round's 32 part tiles, staged once for the CTA's 8 rows (two buffers): row w's
+  // 64-bit key mask of each tile, and the tiles' columns
+  __shared__ __align__(16) uint64_t s_mask[2][kRowWarps][32];
+  __shared__ int s_col[2][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * kRowWarps + warp;
-  if (i >= A.Lq) return;
+  // rows past Lq (only in the last block) skip the work but take part in staging the scan
+  // rounds and in the block's barriers
+  const bool active = i < A.Lq;
   // grid.y = (batch, launch rank): the launch covers heads hmap.order[0 .. n_ranks-1]
   const int bi = blockIdx.y / A.n_ranks;
   const int h = A.hmap.order[blockIdx.y - bi * A.n_ranks];
@@ -114,7 +120,10 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   const int64_t qrow = bh * A.Lq + i;
   const int64_t kv0 = bh * A.Lk;  // first K/V row of this (b, h)
   float qd[E];                     // this lane's dimensions of q, pre-scaled
-  IO::load_lane(A.q, qrow, lane, qd);
+  if (active) IO::load_lane(A.q, qrow, lane, qd);
+  else
+#pragma unroll
+    for (int e = 0; e < E; ++e) qd[e] = 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     qd[e] *= A.scale_log2;
@@ -122,7 +131,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   }
   __syncwarp();
   const float* sq = s_q[warp];
-  const int a = i >> 6, r = i & 63;
+  // the block's 8 rows lie in one 64-row outer-tile row (8-aligned): same CSR ranges for all
+  const int a = (blockIdx.x * kRowWarps) >> 6, r = i & 63;
   const int64_t mrow = (int64_t)hm * A.mask.ot_rows + a;
   // CSR ranges clamped to the arrays (a damaged mask cannot send the loops past them)
   const int fb = max(A.mask.full_row_ptr[mrow], 0), fe = (int)min((int64_t)A.mask.full_row_ptr[mrow + 1], A.mask.n_full);
@@ -134,7 +144,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
 
   // ---- full tiles: every key in range is valid
-  for (int t = fb; t < fe; ++t) {
+  for (int t = fb; active && t < fe; ++t) {
     // clamped into the mask like the part tiles' columns below
     const int col = (int)min((unsigned)A.mask.full_col_idx[t], (unsigned)A.mask.ot_cols - 1u);
 #pragma unroll 1
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
   // take one update per batch.
   constexpr int LB = E == 2 ? 3 : 2;  // batch of NB = 2^LB keys: 8 at d = 64, 4 at d = 128
   constexpr int NB = 1 << LB;
-  const int wrow = 8 * (r >> 3), sh = (r & 7) * 8;
+  const int wrow = 8 * (r >> 3);  // the row group of the inner-tile words (row w of the block: byte w % 8)
   int* keys = s_keys[warp];
   const int kid = (lane >> (5 - LB)) & (NB - 1);  // key of a batch whose score this lane ends with
   auto batch = [&](int b0, int nb) {
@@ -239,78 +249,111 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
     m = m_new;
   };
   int nk = 0;  // keys waiting in the list (fewer than NB after every flush)
-  for (int t0 = pb; t0 < pe; t0 += 32) {
-    const int tt = t0 + lane;
-    uint64_t bits = 0;
-    int64_t base = 0;
-    if (tt < pe) {
-      const uint4* wp = reinterpret_cast<const uint4*>(A.mask.part_bitmap + (int64_t)tt * 64 + wrow);
-      uint4 w4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) w4[u] = __ldg(wp + u);
-      // byte r % 8 of word 8p + q -> bits 8q..8q+7 of the row's mask (words q = 2u, 2u + 1)
-      const int lo_sh = sh & 31;
-      const bool upper = sh >= 32;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t b0 = ((upper ? w4[u].y : w4[u].x) >> lo_sh) & 0xFFu;
-        const uint32_t b1 = ((upper ? w4[u].w : w4[u].z) >> lo_sh) & 0xFFu;
-        bits |= (uint64_t)(b0 | (b1 << 8)) << (16 * u);
-      }
+  // Staging of a round (tiles t0 .. t0 + 31): thread 4t + u (t < 32, u < 4) loads words 2u and
+  // 2u + 1 of the block's row group of tile t0 + t (16 contiguous bytes; four threads cover
+  // the tile's 64) and writes, for every row w of the block, byte w % 4 of the words' low
+  // (w < 4) or high halves, as bits 16u .. 16u + 15 of row w's mask of that tile; warp 4 loads
+  // the 32 columns. The next round's loads are issued before the current round is scored.
+  const int tid = threadIdx.x;
+  uint4 stw = make_uint4(0u, 0u, 0u, 0u);
+  int stc = 0;
+  auto stage_load = [&](int t0) {
+    if (tid < 128) {
+      const int tt = t0 + (tid >> 2);
+      stw = tt < pe ? __ldg(reinterpret_cast<const uint4*>(A.mask.part_bitmap + (int64_t)tt * 64 + wrow) + (tid & 3))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    } else if (warp == 4) {
+      const int tt = t0 + lane;
+      stc = tt < pe ? __ldg(A.mask.part_col_idx + tt) : 0;
+    }
+  };
+  auto stage_store = [&](int buf) {
+    if (tid < 128) {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(s_mask[buf]) + tid;  // row w: + w * 128
+      const uint32_t p01 = __byte_perm(stw.x, stw.z, 0x5140), p23 = __byte_perm(stw.x, stw.z, 0x7362);
+      const uint32_t p45 = __byte_perm(stw.y, stw.w, 0x5140), p67 = __byte_perm(stw.y, stw.w, 0x7362);
+      dst[0 * 128] = (uint16_t)p01;
+      dst[1 * 128] = (uint16_t)(p01 >> 16);
+      dst[2 * 128] = (uint16_t)p23;
+      dst[3 * 128] = (uint16_t)(p23 >> 16);
+      dst[4 * 128] = (uint16_t)p45;
+      dst[5 * 128] = (uint16_t)(p45 >> 16);
+      dst[6 * 128] = (uint16_t)p67;
+      dst[7 * 128] = (uint16_t)(p67 >> 16);
+    } else if (warp == 4) {
+      s_col[buf][lane] = stc;
+    }
+  };
+  if (pb < pe) {
+    stage_load(pb);
+    stage_store(0);
+  }
+  __syncthreads();
+  int buf = 0;
+  for (int t0 = pb; t0 < pe; t0 += 32) {  // the same rounds in every warp of the block
+    const bool more = t0 + 32 < pe;
+    if (more) stage_load(t0 + 32);
+    if (active) {
+      const uint64_t bits = s_mask[buf][warp][lane];  // 0 past the row's last part tile
       // column and key clamped into the mask: a damaged mask (sta_validate_mask finds it)
       // gives wrong values but no read outside K and V
-      base = (int64_t)min((unsigned)__ldg(A.mask.part_col_idx + tt), (unsigned)A.mask.ot_cols - 1u) * 64;
-    }
-    // all keys of the round at once when they fit the list: each lane writes its tile's keys
-    // at the prefix of the lanes below it (the same ascending order as one tile at a time)
-    const int cnt = __popcll(bits);
-    int incl = cnt;
+      const int64_t base = (int64_t)min((unsigned)s_col[buf][lane], (unsigned)A.mask.ot_cols - 1u) * 64;
+      // all keys of the round at once when they fit the list: each lane writes its tile's keys
+      // at the prefix of the lanes below it (the same ascending order as one tile at a time)
+      const int cnt = __popcll(bits);
+      int incl = cnt;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (nk + total <= 72) {
-      int pos = nk + incl - cnt;
-      for (uint64_t bm = bits; bm; bm &= bm - 1) keys[pos++] = (int)min(base + (__ffsll(bm) - 1), (int64_t)A.Lk - 1);
-      nk += total;
-      __syncwarp();
-      if (nk >= NB) {
-        int b0 = 0;
-        for (; nk - b0 >= NB; b0 += NB) batch(b0, NB);
-        const int left = nk - b0;
-        const int kl = lane < left ? keys[b0 + lane] : 0;
-        __syncwarp();
-        if (lane < left) keys[lane] = kl;
-        nk = left;
-        __syncwarp();
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      continue;
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (nk + total <= 72) {
+        int pos = nk + incl - cnt;
+        for (uint64_t bm = bits; bm; bm &= bm - 1) keys[pos++] = (int)min(base + (__ffsll(bm) - 1), (int64_t)A.Lk - 1);
+        nk += total;
+        __syncwarp();
+        if (nk >= NB) {
+          int b0 = 0;
+          for (; nk - b0 >= NB; b0 += NB) batch(b0, NB);
+          const int left = nk - b0;
+          const int kl = lane < left ? keys[b0 + lane] : 0;
+          __syncwarp();
+          if (lane < left) keys[lane] = kl;
+          nk = left;
+          __syncwarp();
+        }
+      } else {
+        for (unsigned nz = __ballot_sync(0xffffffffu, bits != 0ull); nz; nz &= nz - 1) {
+          const int src = __ffs(nz) - 1;
+          const uint64_t mb64 = __shfl_sync(0xffffffffu, bits, src);
+          const int64_t bs = __shfl_sync(0xffffffffu, base, src);
+          // lane c appends keys c and c + 32 of this tile when valid, in ascending order
+          const uint32_t lo = (uint32_t)mb64, hi = (uint32_t)(mb64 >> 32);
+          const uint32_t below = (1u << lane) - 1u;
+          if ((lo >> lane) & 1u) keys[nk + __popc(lo & below)] = (int)min(bs + lane, (int64_t)A.Lk - 1);
+          if ((hi >> lane) & 1u) keys[nk + __popc(lo) + __popc(hi & below)] = (int)min(bs + 32 + lane, (int64_t)A.Lk - 1);
+          nk += __popc(lo) + __popc(hi);
+          __syncwarp();
+          if (nk < NB) continue;
+          int b0 = 0;
+          for (; nk - b0 >= NB; b0 += NB) batch(b0, NB);
+          // the (fewer than NB) keys left over move to the front of the list
+          const int left = nk - b0;
+          const int kl = lane < left ? keys[b0 + lane] : 0;
+          __syncwarp();
+          if (lane < left) keys[lane] = kl;
+          nk = left;
+          __syncwarp();
+        }
+      }
     }
-    for (unsigned nz = __ballot_sync(0xffffffffu, bits != 0ull); nz; nz &= nz - 1) {
-      const int src = __ffs(nz) - 1;
-      const uint64_t mb64 = __shfl_sync(0xffffffffu, bits, src);
-      const int64_t bs = __shfl_sync(0xffffffffu, base, src);
-      // lane c appends keys c and c + 32 of this tile when valid, in ascending order
-      const uint32_t lo = (uint32_t)mb64, hi = (uint32_t)(mb64 >> 32);
-      const uint32_t below = (1u << lane) - 1u;
-      if ((lo >> lane) & 1u) keys[nk + __popc(lo & below)] = (int)min(bs + lane, (int64_t)A.Lk - 1);
-      if ((hi >> lane) & 1u) keys[nk + __popc(lo) + __popc(hi & below)] = (int)min(bs + 32 + lane, (int64_t)A.Lk - 1);
-      nk += __popc(lo) + __popc(hi);
-      __syncwarp();
-      if (nk < NB) continue;
-      int b0 = 0;
-      for (; nk - b0 >= NB; b0 += NB) batch(b0, NB);
-      // the (fewer than NB) keys left over move to the front of the list
-      const int left = nk - b0;
-      const int kl = lane < left ? keys[b0 + lane] : 0;
-      __syncwarp();
-      if (lane < left) keys[lane] = kl;
-      nk = left;
-      __syncwarp();
-    }
+    // the other buffer was last read in the previous round, before that round's barrier
+    if (more) stage_store(buf ^ 1);
+    __syncthreads();
+    buf ^= 1;
   }
+  if (!active) return;
   if (nk > 0) batch(0, nk);
 
   float out[E];
