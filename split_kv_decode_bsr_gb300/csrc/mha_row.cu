@@ -1,12 +1,14 @@
 // Row-wise masked MHA kernel (STOF, デュアルカーネル戦略 / 行方向カーネル):
 // Q sliced by rows, one warp per query row, warp shuffles for the softmax
-// reductions and no synchronisation between warps. The warp walks only the
-// non-empty outer tiles of its row: full tiles 32 keys at a time (one key per
-// lane), part tiles through the row's bytes of their inner-tile words, skipping
-// empty inner tiles and scoring each valid key with the head dimensions spread
-// over the lanes. Scores fold into an fp32 online softmax (running max m,
-// running sum l, output rescaled by exp2(m_old - m_new)). Handles bf16 and fp32
-// inputs, head dims 64 and 128.
+// reductions. The warp walks only the non-empty outer tiles of its row: full
+// tiles 32 keys at a time (one key per lane), part tiles through the row's bytes
+// of their inner-tile words, skipping empty inner tiles and scoring each valid
+// key with the head dimensions spread over the lanes. Scores fold into an fp32
+// online softmax (running max m, running sum l, output rescaled by
+// exp2(m_old - m_new)). Handles bf16 and fp32 inputs, head dims 64 and 128.
+// Unlike the pages' kernel, the warps of a block are not independent: its 8 rows
+// need the same inner-tile words, which the block stages once per round of 32
+// part tiles (one block barrier per round) instead of every warp loading them.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -143,6 +145,45 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
 
+  // Staging of a round (tiles t0 .. t0 + 31): thread 4t + u (t < 32, u < 4) loads words 2u and
+  // 2u + 1 of the block's row group of tile t0 + t (16 contiguous bytes; four threads cover
+  // the tile's 64) and writes, for every row w of the block, byte w % 4 of the words' low
+  // (w < 4) or high halves, as bits 16u .. 16u + 15 of row w's mask of that tile; warp 4 loads
+  // the 32 columns. The next round's loads are issued before the current round is scored.
+  const int wrow = 8 * (r >> 3);  // the row group of the inner-tile words (row w of the block: byte w % 8)
+  const int tid = threadIdx.x;
+  uint4 stw = make_uint4(0u, 0u, 0u, 0u);
+  int stc = 0;
+  auto stage_load = [&](int t0) {
+    if (tid < 128) {
+      const int tt = t0 + (tid >> 2);
+      stw = tt < pe ? __ldg(reinterpret_cast<const uint4*>(A.mask.part_bitmap + (int64_t)tt * 64 + wrow) + (tid & 3))
+                    : make_uint4(0u, 0u, 0u, 0u);
+    } else if (warp == 4) {
+      const int tt = t0 + lane;
+      stc = tt < pe ? __ldg(A.mask.part_col_idx + tt) : 0;
+    }
+  };
+  auto stage_store = [&](int buf) {
+    if (tid < 128) {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(s_mask[buf]) + tid;  // row w: + w * 128
+      const uint32_t p01 = __byte_perm(stw.x, stw.z, 0x5140), p23 = __byte_perm(stw.x, stw.z, 0x7362);
+      const uint32_t p45 = __byte_perm(stw.y, stw.w, 0x5140), p67 = __byte_perm(stw.y, stw.w, 0x7362);
+      dst[0 * 128] = (uint16_t)p01;
+      dst[1 * 128] = (uint16_t)(p01 >> 16);
+      dst[2 * 128] = (uint16_t)p23;
+      dst[3 * 128] = (uint16_t)(p23 >> 16);
+      dst[4 * 128] = (uint16_t)p45;
+      dst[5 * 128] = (uint16_t)(p45 >> 16);
+      dst[6 * 128] = (uint16_t)p67;
+      dst[7 * 128] = (uint16_t)(p67 >> 16);
+    } else if (warp == 4) {
+      s_col[buf][lane] = stc;
+    }
+  };
+  // the first round's loads are in flight while the full tiles are scored
+  if (pb < pe) stage_load(pb);
+
   // ---- full tiles: every key in range is valid
   for (int t = fb; active && t < fe; ++t) {
     // clamped into the mask like the part tiles' columns below
@@ -182,18 +223,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
     }
   }
 
-  // ---- part tiles, 32 at a time: lane l takes part tile t0 + l and loads the row's group
-  // of its inner-tile words (eight words, 64 contiguous bytes) in four 16-byte loads, so
-  // the scan of 32 tiles costs one round trip; byte r % 8 of the eight words is the row's
-  // 64-bit key mask of that tile. The valid keys of each lane with a nonzero mask are then
-  // appended to a list in shared memory (one key per lane per step), and the list is
-  // scored NB keys at a time: every lane loads its dimensions of all NB K and V rows at
-  // once, the NB dot products are reduced together (a transpose-reduce that leaves key
-  // (lane >> (5 - LB)) of the batch on its lanes), and the running max, sum and output
-  // take one update per batch.
+  // ---- part tiles, 32 per round: lane l takes part tile t0 + l, whose 64-bit key mask for
+  // this row (byte r % 8 of the row group's eight inner-tile words) the block has staged in
+  // shared memory. The valid keys of the round are appended to the warp's list in shared
+  // memory, and the list is scored NB keys at a time: every lane loads its dimensions of all
+  // NB K and V rows at once, the NB dot products are reduced together (a transpose-reduce
+  // that leaves key (lane >> (5 - LB)) of the batch on its lanes), and the running max, sum
+  // and output take one update per batch.
   constexpr int LB = E == 2 ? 3 : 2;  // batch of NB = 2^LB keys: 8 at d = 64, 4 at d = 128
   constexpr int NB = 1 << LB;
-  const int wrow = 8 * (r >> 3);  // the row group of the inner-tile words (row w of the block: byte w % 8)
   int* keys = s_keys[warp];
   const int kid = (lane >> (5 - LB)) & (NB - 1);  // key of a batch whose score this lane ends with
   auto batch = [&](int b0, int nb) {
@@ -249,45 +287,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) mha_row_kernel(const MhaArgs A
     m = m_new;
   };
   int nk = 0;  // keys waiting in the list (fewer than NB after every flush)
-  // Staging of a round (tiles t0 .. t0 + 31): thread 4t + u (t < 32, u < 4) loads words 2u and
-  // 2u + 1 of the block's row group of tile t0 + t (16 contiguous bytes; four threads cover
-  // the tile's 64) and writes, for every row w of the block, byte w % 4 of the words' low
-  // (w < 4) or high halves, as bits 16u .. 16u + 15 of row w's mask of that tile; warp 4 loads
-  // the 32 columns. The next round's loads are issued before the current round is scored.
-  const int tid = threadIdx.x;
-  uint4 stw = make_uint4(0u, 0u, 0u, 0u);
-  int stc = 0;
-  auto stage_load = [&](int t0) {
-    if (tid < 128) {
-      const int tt = t0 + (tid >> 2);
-      stw = tt < pe ? __ldg(reinterpret_cast<const uint4*>(A.mask.part_bitmap + (int64_t)tt * 64 + wrow) + (tid & 3))
-                    : make_uint4(0u, 0u, 0u, 0u);
-    } else if (warp == 4) {
-      const int tt = t0 + lane;
-      stc = tt < pe ? __ldg(A.mask.part_col_idx + tt) : 0;
-    }
-  };
-  auto stage_store = [&](int buf) {
-    if (tid < 128) {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(s_mask[buf]) + tid;  // row w: + w * 128
-      const uint32_t p01 = __byte_perm(stw.x, stw.z, 0x5140), p23 = __byte_perm(stw.x, stw.z, 0x7362);
-      const uint32_t p45 = __byte_perm(stw.y, stw.w, 0x5140), p67 = __byte_perm(stw.y, stw.w, 0x7362);
-      dst[0 * 128] = (uint16_t)p01;
-      dst[1 * 128] = (uint16_t)(p01 >> 16);
-      dst[2 * 128] = (uint16_t)p23;
-      dst[3 * 128] = (uint16_t)(p23 >> 16);
-      dst[4 * 128] = (uint16_t)p45;
-      dst[5 * 128] = (uint16_t)(p45 >> 16);
-      dst[6 * 128] = (uint16_t)p67;
-      dst[7 * 128] = (uint16_t)(p67 >> 16);
-    } else if (warp == 4) {
-      s_col[buf][lane] = stc;
-    }
-  };
-  if (pb < pe) {
-    stage_load(pb);
-    stage_store(0);
-  }
+  if (pb < pe) stage_store(0);
   __syncthreads();
   int buf = 0;
   for (int t0 = pb; t0 < pe; t0 += 32) {  // the same rounds in every warp of the block
