@@ -64,14 +64,19 @@ def load_peaks():
 
 
 def kernel_source_sha(name: str) -> str:
-    """sha1 (12 hex) of a kernel source with comments and whitespace removed: edits to comments
-    keep recorded counters valid, any code change invalidates them."""
-    p = os.path.join(ROOT, "split_kv_decode_bsr_gb300", "csrc", name)
-    src = open(p, encoding="utf-8").read()
-    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-    src = re.sub(r"//[^\n]*", " ", src)
-    src = re.sub(r"\s+", " ", src).strip()
-    return hashlib.sha1(src.encode()).hexdigest()[:12]
+    """sha1 (12 hex) of a kernel source and of the library's headers (the `.cuh` / `.h` files
+    beside it, which every kernel file includes), comments and whitespace removed: edits to
+    comments keep recorded counters valid, any code change in the file or a header invalidates
+    them."""
+    d = os.path.join(ROOT, "split_kv_decode_bsr_gb300", "csrc")
+    files = [name] + sorted(f for f in os.listdir(d) if f.endswith((".cuh", ".h")))
+    h = hashlib.sha1()
+    for f in files:
+        src = open(os.path.join(d, f), encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(re.sub(r"\s+", " ", src).strip().encode() + b"\0")
+    return h.hexdigest()[:12]
 
 
 def recorded_traffic(kernel_file: str, workload: str):

@@ -54,11 +54,12 @@ struct MaskView {
 // Row r (0..63) of a part outer tile: 64-bit key mask, bit c = column c of the tile.
 // Byte (r % 8) of IT word 8*(r/8) + q holds columns 8q..8q+7 of that row.
 __device__ __forceinline__ uint64_t part_row_bits(const uint64_t* words, int r) {
-  const int p = r >> 3, sh = (r & 7) * 8;
-  uint64_t m = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) m |= ((words[8 * p + q] >> sh) & 0xFFull) << (8 * q);
-  return m;
+  // the 32-bit half of each word that holds byte r % 8, then byte r % 4 of each gathered
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(words + 8 * (r >> 3)) + ((r >> 2) & 1);
+  const uint32_t b = (uint32_t)(r & 3), sel = b | ((4u + b) << 4);
+  const uint32_t x01 = __byte_perm(w[0], w[2], sel), x23 = __byte_perm(w[4], w[6], sel);
+  const uint32_t x45 = __byte_perm(w[8], w[10], sel), x67 = __byte_perm(w[12], w[14], sel);
+  return (uint64_t)__byte_perm(x01, x23, 0x5410) | ((uint64_t)__byte_perm(x45, x67, 0x5410) << 32);
 }
 
 // Merge s partials of one row; lane owns E consecutive dims. po points at the

@@ -36,6 +36,15 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_sha("epilogue.cu") == h0
     (csrc / "epilogue.cu").write_text(text.replace("constexpr int kMaxVec = 4;", "constexpr int kMaxVec = 2;"))
     assert bench.kernel_source_sha("epilogue.cu") != h0
+    # a code change in a header the kernels include invalidates the record as well
+    (csrc / "epilogue.cu").write_text(text)
+    (csrc / "common.cuh").write_text("// helpers\ninline int f() { return 1; }\n")
+    h1 = bench.kernel_source_sha("epilogue.cu")
+    assert h1 != h0
+    (csrc / "common.cuh").write_text("/* helpers */ inline int f() {\n  return 1;\n}\n")
+    assert bench.kernel_source_sha("epilogue.cu") == h1
+    (csrc / "common.cuh").write_text("inline int f() { return 2; }\n")
+    assert bench.kernel_source_sha("epilogue.cu") != h1
 
 
 def test_recorded_traffic_needs_the_matching_source(tmp_path, monkeypatch):
