@@ -59,6 +59,23 @@ def test_random_masks_ragged(dev, kernel, d, Lq, Lk, density):
     _run(q, k, v, heads, [1, 0, 1], 1.0 / math.sqrt(d), "bf16", kernel, dev, Lq, Lk)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("density", [0.004, 0.05])
+def test_row_kernel_staged_scan_rounds_and_partial_last_block(dev, dtype, d, density):
+    # the row kernel stages each round of 32 part tiles once for a block's 8 rows: Lk = 2400
+    # gives rows 38 part tiles (two rounds), at 5 % a round's keys overflow the list (the
+    # tile-by-tile fallback), the causal-window head adds full tiles before the scan, and
+    # Lq = 2052 leaves 4 rows of the last block past Lq (they stage tiles but score nothing)
+    Lq, Lk, H = 2052, 2400, 2
+    q = W.make_tensor(11, 1, (1, H, Lq, d), dtype)
+    k = W.make_tensor(11, 2, (1, H, Lk, d), dtype)
+    v = W.make_tensor(11, 3, (1, H, Lk, d), dtype)
+    heads = [W.MaskHead("bits", data=W.random_mask_bits(12, 6, Lq, Lk, density)),
+             W.pattern(causal=True, win_lo=-200, win_hi=0, n_global_cols=3)]
+    _run(q, k, v, heads, [0, 1], 1.0 / math.sqrt(d), dtype, "row", dev, Lq, Lk)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Lq,Lk,density", [(200, 300, 0.05), (77, 1000, 0.3), (130, 65, 1.0)])
 def test_block_kernel_builds_its_own_column_lists(dev, d, Lq, Lk, density):
